@@ -1,0 +1,116 @@
+// Host-side planning of streaming GEMV launches: K split, rows per CTA,
+// grid and the dynamic shared-memory layout.
+#pragma once
+
+#include <algorithm>
+
+#include "gemv_kernel.cuh"
+#include "phb_internal.h"
+
+namespace phb {
+
+inline int maxb_for(int batch) { return batch <= 1 ? 1 : batch <= 2 ? 2 : batch <= 4 ? 4 : 8; }
+
+constexpr size_t kXSmemBudget = 80 * 1024;  // activations staged per CTA before K is split
+
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Number of K splits for a request (1 unless the staged activations would
+// not fit the per-CTA budget).
+inline int plan_ksplit(const GemvReq& q) {
+    const int units_row = static_cast<int>(q.k / kUnitWeights);
+    if (q.nmat != 1 || q.xmode != kXPlain || q.epi != kEpiStore) return 1;
+    const size_t xbytes = static_cast<size_t>(q.batch) * q.k * sizeof(float);
+    int ks = static_cast<int>(cdiv(static_cast<int64_t>(xbytes), kXSmemBudget));
+    ks = std::max(1, std::min(ks, units_row));
+    const int seg = static_cast<int>(cdiv(units_row, ks));
+    return static_cast<int>(cdiv(units_row, seg));
+}
+
+// Dynamic shared memory of a streaming-GEMV CTA:
+//   stages | xs [batch][xpad_len(kseg)] | xsum [batch][kseg/32] |
+//   part [kAccStride][256] | row_acc [nmat*rows][kAccStride] | mbarriers | red | xfac | row list
+struct SmemLayout {
+    uint32_t xs, xsum, part, acc, bar;
+    size_t total;
+};
+
+inline SmemLayout stream_smem_layout(int qt, int nmat, int xrows, int rows_per_cta, int units_seg) {
+    const int ub = qt == 0 ? Fmt<0>::unit_bytes : Fmt<1>::unit_bytes;
+    const int ns = qt == 0 ? StageCfg<0>::ns : StageCfg<1>::ns;
+    SmemLayout l{};
+    size_t off = static_cast<size_t>(ns) * kStageUnits * ub;
+    const size_t kseg = static_cast<size_t>(units_seg) * kUnitWeights;
+    l.xs = static_cast<uint32_t>(off);
+    off += static_cast<size_t>(xrows) * xpad_len(static_cast<int>(kseg)) * sizeof(float);
+    l.xsum = static_cast<uint32_t>(off);
+    off += static_cast<size_t>(xrows) * (kseg / 32) * sizeof(float);
+    l.part = static_cast<uint32_t>(off);
+    off += static_cast<size_t>(2 * kStageUnits) * kAccStride * sizeof(float);
+    l.acc = static_cast<uint32_t>(off);
+    off += static_cast<size_t>(nmat) * rows_per_cta * kAccStride * sizeof(float);
+    l.bar = static_cast<uint32_t>(off);
+    off += 2 * ns * sizeof(uint64_t);
+    off += static_cast<size_t>(kConsumerWarps + 3) * kAccStride * sizeof(float);  // red, xfac, row list
+    l.total = off;
+    return l;
+}
+
+// Fill a launch plan. Returns false if no layout fits shared memory.
+inline bool plan_stream(const GemvReq& q, GemvPlan* pl) {
+    const int units_row = static_cast<int>(q.k / kUnitWeights);
+    const int ksplit0 = plan_ksplit(q);
+    const int units_seg = static_cast<int>(cdiv(units_row, ksplit0));
+    const int ksplit = static_cast<int>(cdiv(units_row, units_seg));
+    const int maxb = maxb_for(q.batch);
+    const int sms = device_sm_count();
+    const int64_t target = std::max<int64_t>(1, cdiv(2 * static_cast<int64_t>(sms), ksplit));
+    int64_t nrow_ctas = std::min<int64_t>(q.n, target);
+    int rows_per_cta = static_cast<int>(cdiv(q.n, nrow_ctas));
+    SmemLayout lay{};
+    for (;;) {
+        lay = stream_smem_layout(q.qt, q.nmat, q.batch, rows_per_cta, units_seg);
+        if (lay.total <= kSmemOptin) break;
+        if (rows_per_cta == 1) return false;
+        rows_per_cta = (rows_per_cta + 1) / 2;
+    }
+    nrow_ctas = cdiv(q.n, rows_per_cta);
+    GemvParams& p = pl->p;
+    p = GemvParams{};
+    p.w[0] = static_cast<const uint8_t*>(q.w0);
+    p.w[1] = static_cast<const uint8_t*>(q.nmat == 2 ? q.w1 : q.w0);
+    p.row_bytes = static_cast<int64_t>(units_row) * (q.qt == 0 ? Fmt<0>::unit_bytes : Fmt<1>::unit_bytes);
+    p.n = q.n;
+    p.units_row = units_row;
+    p.units_seg = units_seg;
+    p.rows_per_cta = rows_per_cta;
+    p.batch = q.batch;
+    p.x = q.x;
+    p.ldx = q.ldx;
+    p.y = q.y;
+    p.ldy = q.ldy;
+    p.r = q.r;
+    p.ldr = q.ldr;
+    p.part = q.ws;
+    p.gather_group = q.gather_group;
+    p.gather_hd = q.gather_hd;
+    p.gather_v_off = q.gather_v_off;
+    p.xs_off = lay.xs;
+    p.xsum_off = lay.xsum;
+    p.part_off = lay.part;
+    p.acc_off = lay.acc;
+    p.bar_off = lay.bar;
+    pl->grid = dim3(static_cast<unsigned>(nrow_ctas), static_cast<unsigned>(ksplit), 1);
+    pl->smem = lay.total;
+    return true;
+}
+
+template <int QT, int MAXB, int NMAT, int XMODE, int EPI>
+inline cudaError_t run_stream(const GemvPlan& pl, cudaStream_t s, bool pdl) {
+    constexpr auto kern = gemv_stream_kernel<QT, MAXB, NMAT, XMODE, EPI>;
+    cudaError_t e = ensure_smem_attr<kern>();
+    if (e != cudaSuccess) return e;
+    return launch_kernel(kern, pl.grid, dim3(kGemvThreads), pl.smem, s, pdl, pl.p);
+}
+
+}  // namespace phb

@@ -1,0 +1,389 @@
+// Top-k routed mixture-of-experts FFN.
+//
+// 1. moe_route_kernel (one CTA): per token the top_k largest router logits
+//    (ties to the lower expert index) and their softmax; then a counting sort
+//    of the (token, slot) pairs by expert, ascending pair id within an
+//    expert, giving the active-expert list.
+// 2. moe_stream_kernel<NMAT=2>: grid (CTAs per expert, expert slot). Each CTA
+//    streams a row range of its expert's gate and up matrices once and
+//    applies it to every token routed to that expert (groups of up to 8),
+//    writing h[pair] = silu(gate.x) * (up.x).
+// 3. moe_stream_kernel<NMAT=1>: the same over the down matrices, x = h[pair],
+//    writing y_pair[pair].
+// 4. moe_combine_kernel: y[t] = sum over slots (ascending) of p[t][slot] *
+//    y_pair[t*top_k + slot].
+// All orders are fixed, so repeated calls give identical bits.
+#include <algorithm>
+#include <cfloat>
+#include <cmath>
+
+#include "gemv_plan.cuh"
+#include "phb_internal.h"
+
+namespace phb {
+
+cudaError_t read_dev_err_moe(int* code) {
+    int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_dev_err, sizeof(int));
+    if (e != cudaSuccess) return e;
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_dev_err, &zero, sizeof(int));
+    *code = v;
+    return e;
+}
+
+namespace {
+
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopK = 8;
+constexpr int kMaxTokens = 64;
+constexpr int kMoeGroup = 8;  // tokens per pass over a staged weight tile
+
+struct RouteOut {
+    int32_t* idx;        // [T][k]
+    float* p;            // [T][k]
+    int32_t* n_active;   // [1]
+    int32_t* act_expert; // [slots]
+    int32_t* act_off;    // [slots]
+    int32_t* act_cnt;    // [slots]
+    int32_t* pair_list;  // [T*k]
+};
+
+__global__ void __launch_bounds__(256) moe_route_kernel(const float* __restrict__ logits, int T, int E, int K,
+                                                        RouteOut o, int32_t* out_idx, float* out_p) {
+    pdl_launch_dependents();
+    pdl_wait();
+    __shared__ int32_t sidx[kMaxTokens * kMaxTopK];
+    __shared__ int32_t cnt[kMaxExperts];
+    __shared__ int32_t off[kMaxExperts];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nwarps = blockDim.x >> 5;
+    for (int t = warp; t < T; t += nwarps) {
+        float v[kMaxExperts / 32];
+        uint32_t taken = 0;
+#pragma unroll
+        for (int j = 0; j < kMaxExperts / 32; ++j) {
+            const int e = lane + 32 * j;
+            v[j] = e < E ? logits[static_cast<int64_t>(t) * E + e] : -FLT_MAX;
+        }
+        float sel_v[kMaxTopK];
+        int sel_e[kMaxTopK];
+        for (int r = 0; r < K; ++r) {
+            float bv = -FLT_MAX;
+            int be = 0x7FFFFFFF;
+#pragma unroll
+            for (int j = 0; j < kMaxExperts / 32; ++j) {
+                const int e = lane + 32 * j;
+                if (e < E && !((taken >> j) & 1u) && (v[j] > bv || (v[j] == bv && e < be))) {
+                    bv = v[j];
+                    be = e;
+                }
+            }
+#pragma unroll
+            for (int s = 16; s > 0; s >>= 1) {
+                const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, s);
+                const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, s);
+                if (ov > bv || (ov == bv && oe < be)) {
+                    bv = ov;
+                    be = oe;
+                }
+            }
+            if ((be & 31) == lane) taken |= 1u << (be >> 5);
+            sel_v[r] = bv;
+            sel_e[r] = be;
+        }
+        if (lane == 0) {
+            float ex[kMaxTopK];
+            float sum = 0.f;
+            for (int r = 0; r < K; ++r) {
+                ex[r] = expf(sel_v[r] - sel_v[0]);
+                sum += ex[r];
+            }
+            for (int r = 0; r < K; ++r) {
+                const float pr = ex[r] / sum;
+                const int q = t * K + r;
+                sidx[q] = sel_e[r];
+                o.idx[q] = sel_e[r];
+                o.p[q] = pr;
+                if (out_idx) out_idx[q] = sel_e[r];
+                if (out_p) out_p[q] = pr;
+            }
+        }
+    }
+    __syncthreads();
+    const int pairs = T * K;
+    for (int e = tid; e < E; e += blockDim.x) {
+        int c = 0;
+        for (int q = 0; q < pairs; ++q) c += (sidx[q] == e);
+        cnt[e] = c;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int a = 0, acc = 0;
+        for (int e = 0; e < E; ++e) {
+            off[e] = acc;
+            if (cnt[e] > 0) {
+                o.act_expert[a] = e;
+                o.act_off[a] = acc;
+                o.act_cnt[a] = cnt[e];
+                ++a;
+                acc += cnt[e];
+            }
+        }
+        *o.n_active = a;
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += blockDim.x) {
+        if (cnt[e] == 0) continue;
+        int w = off[e];
+        for (int q = 0; q < pairs; ++q)
+            if (sidx[q] == e) o.pair_list[w++] = q;
+    }
+}
+
+struct MoeParams {
+    const uint8_t* w[2];      // expert 0 of each matrix
+    int64_t expert_stride;    // bytes per expert matrix
+    int64_t row_bytes;
+    int64_t n;                // rows per expert matrix
+    int units_row;
+    int rows_per_cta;
+    const float* x;           // gate/up: X [T][K]; down: h [pairs][K]
+    int64_t ldx;
+    int x_by_pair;            // 0: x row = pair / top_k; 1: x row = pair
+    int top_k;
+    float* y;                 // [pairs][n]
+    int64_t ldy;
+    RouteOut r;
+    uint32_t xs_off, xsum_off, part_off, acc_off, bar_off;
+};
+
+template <int QT, int NMAT, int MAXB>
+__device__ __forceinline__ bool moe_group(const MoeParams& p, const Tile& t, int row0, int first_pair_idx, int nb,
+                                          uint8_t* smem, uint64_t* full, uint64_t* empty, int& s) {
+    float* xs = reinterpret_cast<float*>(smem + p.xs_off);
+    float* xsum = reinterpret_cast<float*>(smem + p.xsum_off);
+    float* part = reinterpret_cast<float*>(smem + p.part_off);
+    float* row_acc = reinterpret_cast<float*>(smem + p.acc_off);
+    float* red = reinterpret_cast<float*>(smem + p.bar_off + 2 * StageCfg<QT>::ns * sizeof(uint64_t));
+    float* xfac = red + (kConsumerWarps + 1) * kAccStride;
+    int* rowidx = reinterpret_cast<int*>(xfac + kAccStride);
+    const int tid = threadIdx.x;
+    const int kseg = t.useg * kUnitWeights;
+    if (tid < nb) {
+        const int pair = p.r.pair_list[first_pair_idx + tid];
+        rowidx[tid] = p.x_by_pair ? pair : pair / p.top_k;
+    }
+    for (int i = tid; i < NMAT * t.rows_here * kAccStride; i += kConsumers) row_acc[i] = 0.f;
+    consumer_sync();
+    stage_x<QT, MAXB, kXRowList>(p.x, p.ldx, 0, kseg, nb, xs, xsum, xfac, red, 1, 1, 0, rowidx);
+    if (!consume_tile<QT, MAXB>(t, NMAT, smem, full, empty, s, xs, xpad_len(kseg), xsum, kseg / 32, xfac, nb, part,
+                                row_acc))
+        return false;
+    for (int it = tid; it < t.rows_here * nb; it += kConsumers) {
+        const int rr = it / nb;
+        const int b = it - rr * nb;
+        const int pair = p.r.pair_list[first_pair_idx + b];
+        const float a0 = row_acc[rr * kAccStride + b];
+        float out = a0;
+        if constexpr (NMAT == 2) out = silu_mul(a0, row_acc[(t.rows_here + rr) * kAccStride + b]);
+        p.y[static_cast<int64_t>(pair) * p.ldy + row0 + rr] = out;
+    }
+    consumer_sync();
+    return true;
+}
+
+template <int QT, int NMAT>
+__global__ void __launch_bounds__(kGemvThreads, 1) moe_stream_kernel(const __grid_constant__ MoeParams p) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    constexpr int NS = StageCfg<QT>::ns;
+    constexpr int UB = Fmt<QT>::unit_bytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
+    uint64_t* empty = full + NS;
+    pdl_launch_dependents();
+    pdl_wait();  // routing results (and, for the down pass, h) come from the previous kernels
+    const int slot = blockIdx.y;
+    if (slot >= *p.r.n_active) return;
+    const int e = p.r.act_expert[slot];
+    const int first = p.r.act_off[slot];
+    const int cnt = p.r.act_cnt[slot];
+    const int row0 = blockIdx.x * p.rows_per_cta;
+    Tile t;
+    t.rows_here = static_cast<int>(min(static_cast<int64_t>(p.rows_per_cta), p.n - row0));
+    if (t.rows_here <= 0) return;
+    t.useg = p.units_row;
+    t.row_bytes = p.row_bytes;
+    t.contiguous = true;
+    t.w[0] = p.w[0] + e * p.expert_stride + static_cast<int64_t>(row0) * p.row_bytes;
+    t.w[1] = p.w[NMAT - 1] + e * p.expert_stride + static_cast<int64_t>(row0) * p.row_bytes;
+    (void)UB;
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+    const int ngroups = (cnt + kMoeGroup - 1) / kMoeGroup;
+    if (tid >= kConsumers) {
+        if (tid == kConsumers) {
+            const uint64_t pol = policy_evict_first();
+            int s = 0;
+            for (int gi = 0; gi < ngroups; ++gi)
+                if (!produce_tile<QT>(t, NMAT, smem, full, empty, s, pol)) break;
+        }
+        return;
+    }
+    int s = 0;
+    for (int gi = 0; gi < ngroups; ++gi) {
+        const int nb = min(kMoeGroup, cnt - gi * kMoeGroup);
+        const int fp = first + gi * kMoeGroup;
+        bool ok;
+        if (nb == 1)
+            ok = moe_group<QT, NMAT, 1>(p, t, row0, fp, nb, smem, full, empty, s);
+        else if (nb == 2)
+            ok = moe_group<QT, NMAT, 2>(p, t, row0, fp, nb, smem, full, empty, s);
+        else if (nb <= 4)
+            ok = moe_group<QT, NMAT, 4>(p, t, row0, fp, nb, smem, full, empty, s);
+        else
+            ok = moe_group<QT, NMAT, 8>(p, t, row0, fp, nb, smem, full, empty, s);
+        if (!ok) return;
+    }
+}
+
+__global__ void __launch_bounds__(256) moe_combine_kernel(const float* __restrict__ yp, const float* __restrict__ p,
+                                                          float* __restrict__ y, int T, int K, int64_t D) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= static_cast<int64_t>(T) * D) return;
+    const int64_t t = i / D, d = i - t * D;
+    float acc = 0.f;
+    for (int s = 0; s < K; ++s) acc = fmaf(p[t * K + s], yp[(t * K + s) * D + d], acc);
+    y[i] = acc;
+}
+
+struct MoeWs {
+    RouteOut r;
+    float* h;
+    float* yp;
+    size_t bytes;
+};
+
+inline size_t align_up(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+MoeWs moe_ws_layout(const MoeReq& q, void* base) {
+    const size_t pairs = static_cast<size_t>(q.t) * q.top_k;
+    const size_t slots = static_cast<size_t>(std::min<int64_t>(q.e, static_cast<int64_t>(pairs)));
+    auto* b = static_cast<uint8_t*>(base);
+    size_t off = 0;
+    MoeWs w{};
+    auto take = [&](size_t bytes) {
+        uint8_t* ptr = b ? b + off : nullptr;
+        off = align_up(off + bytes);
+        return ptr;
+    };
+    w.r.idx = reinterpret_cast<int32_t*>(take(pairs * 4));
+    w.r.p = reinterpret_cast<float*>(take(pairs * 4));
+    w.r.n_active = reinterpret_cast<int32_t*>(take(16));
+    w.r.act_expert = reinterpret_cast<int32_t*>(take(slots * 4));
+    w.r.act_off = reinterpret_cast<int32_t*>(take(slots * 4));
+    w.r.act_cnt = reinterpret_cast<int32_t*>(take(slots * 4));
+    w.r.pair_list = reinterpret_cast<int32_t*>(take(pairs * 4));
+    w.h = reinterpret_cast<float*>(take(pairs * q.d_ff * 4));
+    w.yp = reinterpret_cast<float*>(take(pairs * q.d_model * 4));
+    w.bytes = off;
+    return w;
+}
+
+template <int QT, int NMAT>
+cudaError_t launch_moe_stream(const MoeParams& p, dim3 grid, size_t smem, cudaStream_t s) {
+    constexpr auto kern = moe_stream_kernel<QT, NMAT>;
+    cudaError_t e = ensure_smem_attr<kern>();
+    if (e != cudaSuccess) return e;
+    return launch_kernel(kern, grid, dim3(kGemvThreads), smem, s, true, p);
+}
+
+// Rows per CTA and shared-memory layout of one grouped pass.
+bool plan_moe(int qt, int nmat, int64_t n, int64_t k, int cpe, MoeParams* p, unsigned* gx, size_t* smem) {
+    const int units_row = static_cast<int>(k / kUnitWeights);
+    int rows_per_cta = static_cast<int>(cdiv(n, cpe));
+    SmemLayout lay{};
+    for (;;) {
+        lay = stream_smem_layout(qt, nmat, kMoeGroup, rows_per_cta, units_row);
+        if (lay.total <= kSmemOptin) break;
+        if (rows_per_cta == 1) return false;
+        rows_per_cta = (rows_per_cta + 1) / 2;
+    }
+    p->units_row = units_row;
+    p->rows_per_cta = rows_per_cta;
+    p->row_bytes = static_cast<int64_t>(units_row) * (qt == 0 ? Fmt<0>::unit_bytes : Fmt<1>::unit_bytes);
+    p->n = n;
+    p->expert_stride = n * p->row_bytes;
+    p->xs_off = lay.xs;
+    p->xsum_off = lay.xsum;
+    p->part_off = lay.part;
+    p->acc_off = lay.acc;
+    p->bar_off = lay.bar;
+    *gx = static_cast<unsigned>(cdiv(n, rows_per_cta));
+    *smem = lay.total;
+    return true;
+}
+
+}  // namespace
+
+size_t moe_ws_bytes(const MoeReq& q) { return moe_ws_layout(q, nullptr).bytes; }
+
+cudaError_t moe_run(const MoeReq& q, cudaStream_t s) {
+    const MoeWs w = moe_ws_layout(q, q.ws);
+    const int pairs = static_cast<int>(q.t * q.top_k);
+    const int slots = std::min(q.e, pairs);
+    cudaError_t e = launch_kernel(moe_route_kernel, dim3(1), dim3(256), 0, s, true, q.logits, static_cast<int>(q.t),
+                                  q.e, q.top_k, w.r, q.out_idx, q.out_p);
+    if (e != cudaSuccess) return e;
+    // CTAs per expert: enough to cover the GPU twice for the expected number
+    // of distinct experts, E * (1 - (1 - k/E)^T).
+    double expected = q.e * (1.0 - std::pow(1.0 - static_cast<double>(q.top_k) / q.e, static_cast<double>(q.t)));
+    expected = std::min<double>(slots, std::max(1.0, expected));
+    const int cpe = std::max(1, static_cast<int>(std::ceil(2.0 * device_sm_count() / expected)));
+
+    MoeParams pg{};
+    unsigned gx = 0;
+    size_t smem = 0;
+    if (!plan_moe(q.qt, 2, q.d_ff, q.d_model, cpe, &pg, &gx, &smem)) return cudaErrorInvalidConfiguration;
+    pg.w[0] = static_cast<const uint8_t*>(q.wg);
+    pg.w[1] = static_cast<const uint8_t*>(q.wu);
+    pg.x = q.x;
+    pg.ldx = q.d_model;
+    pg.x_by_pair = 0;
+    pg.top_k = q.top_k;
+    pg.y = w.h;
+    pg.ldy = q.d_ff;
+    pg.r = w.r;
+    e = q.qt == 0 ? launch_moe_stream<0, 2>(pg, dim3(gx, slots), smem, s)
+                  : launch_moe_stream<1, 2>(pg, dim3(gx, slots), smem, s);
+    if (e != cudaSuccess) return e;
+
+    MoeParams pd{};
+    if (!plan_moe(q.qt, 1, q.d_model, q.d_ff, cpe, &pd, &gx, &smem)) return cudaErrorInvalidConfiguration;
+    pd.w[0] = pd.w[1] = static_cast<const uint8_t*>(q.wd);
+    pd.x = w.h;
+    pd.ldx = q.d_ff;
+    pd.x_by_pair = 1;
+    pd.top_k = q.top_k;
+    pd.y = w.yp;
+    pd.ldy = q.d_model;
+    pd.r = w.r;
+    e = q.qt == 0 ? launch_moe_stream<0, 1>(pd, dim3(gx, slots), smem, s)
+                  : launch_moe_stream<1, 1>(pd, dim3(gx, slots), smem, s);
+    if (e != cudaSuccess) return e;
+
+    const int64_t total = q.t * q.d_model;
+    return launch_kernel(moe_combine_kernel, dim3(static_cast<unsigned>(cdiv(total, 256))), dim3(256), 0, s, true,
+                         static_cast<const float*>(w.yp), static_cast<const float*>(w.r.p), q.y,
+                         static_cast<int>(q.t), q.top_k, q.d_model);
+}
+
+}  // namespace phb

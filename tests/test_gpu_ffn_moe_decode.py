@@ -1,0 +1,212 @@
+"""GPU parity of the SwiGLU FFN, the routed MoE FFN and the dense decode step.
+
+Tolerances are the oracle's propagated bounds (oracle.swiglu_ffn,
+oracle.moe_ffn, oracle.decode_layer) built on the per-GEMV contract
+|err| <= 1e-3 * sum|w x|.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import quantized_decode_gguf_gb300 as phb
+import synth
+from _helpers import assert_within, check_device_clean, ensure_built, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+
+
+# ---------------------------------------------------------------- SwiGLU FFN
+
+FFN_CASES = [
+    ("q8_0", 2048, 5632, 1),   # decode-layer FFN
+    ("q8_0", 2048, 5632, 4),
+    ("q4_k", 2048, 768, 1),    # one MoE expert
+    ("q4_k", 2048, 768, 8),
+    ("q4_k", 2560, 9728, 2),   # 4B-class FFN
+    ("q8_0", 96, 160, 3),      # generic (unfused) path: K % 256 != 0
+    ("q4_k", 256, 512, 8),
+    ("q8_0", 4096, 1024, 8),   # unfused: 8 * 4096 * 4 B > 80 KB of staged activations
+]
+
+
+@pytest.mark.parametrize("qtype,d_model,d_ff,batch", FFN_CASES)
+def test_ffn_swiglu_within_bound(qtype, d_model, d_ff, batch):
+    seed = 400 + d_ff + batch
+    wg = synth.blocks(qtype, seed, 0, d_ff, d_model)
+    wu = synth.blocks(qtype, seed, 1, d_ff, d_model)
+    wd = synth.blocks(qtype, seed, 2, d_model, d_ff)
+    x = synth.normal_f32(seed, 3, (batch, d_model))
+    y = to_host(phb.ffn_swiglu(qtype, to_dev(wg), to_dev(wu), to_dev(wd), to_dev(x), d_model, d_ff))
+    ref, tol, _ = oracle.swiglu_ffn(oracle.dequant(qtype, wg, d_ff, d_model), oracle.dequant(qtype, wu, d_ff, d_model),
+                                    oracle.dequant(qtype, wd, d_model, d_ff), x)
+    assert_within(y, ref, tol, f"ffn {qtype} {d_model}->{d_ff} b{batch}")
+    check_device_clean()
+
+
+def test_ffn_zero_gate_gives_zero():
+    d_model, d_ff = 512, 512
+    wg = synth.q8_0_blocks(410, 0, d_ff, d_model).reshape(d_ff, -1, 34).copy()
+    wg[..., 0:2] = 0                                    # d = 0: gate weights all zero
+    wg = wg.reshape(d_ff, -1)
+    wu = synth.q8_0_blocks(410, 1, d_ff, d_model)
+    wd = synth.q8_0_blocks(410, 2, d_model, d_ff)
+    x = synth.normal_f32(410, 3, (2, d_model))
+    y = to_host(phb.ffn_swiglu("q8_0", to_dev(wg), to_dev(wu), to_dev(wd), to_dev(x), d_model, d_ff))
+    assert np.all(y == 0)
+
+
+# ---------------------------------------------------------------- MoE
+
+def _experts(qtype, seed, e, d_model, d_ff):
+    wg = np.stack([synth.blocks(qtype, seed, 3 * i, d_ff, d_model) for i in range(e)])
+    wu = np.stack([synth.blocks(qtype, seed, 3 * i + 1, d_ff, d_model) for i in range(e)])
+    wd = np.stack([synth.blocks(qtype, seed, 3 * i + 2, d_model, d_ff) for i in range(e)])
+    return wg, wu, wd
+
+
+def _deq_experts(qtype, blobs, rows, cols):
+    return np.stack([oracle.dequant(qtype, b, rows, cols) for b in blobs])
+
+
+def _run_moe(qtype, wg, wu, wd, x, logits, d_model, d_ff, e, k):
+    t = x.shape[0]
+    idx = torch.empty((t, k), dtype=torch.int32, device="cuda")
+    p = torch.empty((t, k), dtype=torch.float32, device="cuda")
+    y = phb.moe_ffn(qtype, to_dev(wg), to_dev(wu), to_dev(wd), to_dev(x), to_dev(logits), d_model, d_ff, e, k,
+                    out_idx=idx, out_p=p)
+    return to_host(y), to_host(idx), to_host(p)
+
+
+MOE_CASES = [
+    ("q4_k", 1, 128, 8, 2048, 768),    # 35B-A3B-class layer, one token
+    ("q4_k", 16, 128, 8, 2048, 768),   # 16 tokens per step
+    ("q4_k", 5, 8, 2, 256, 512),
+    ("q8_0", 7, 16, 4, 512, 256),
+    ("q4_k", 64, 32, 8, 256, 256),     # many tokens per expert (groups of 8)
+]
+
+
+@pytest.mark.parametrize("qtype,t,e,k,d_model,d_ff", MOE_CASES)
+def test_moe_ffn_within_bound(qtype, t, e, k, d_model, d_ff):
+    seed = 500 + t + e
+    wg, wu, wd = _experts(qtype, seed, e, d_model, d_ff)
+    x = synth.normal_f32(seed, 10_000, (t, d_model))
+    logits = synth.normal_f32(seed, 10_001, (t, e))
+    y, idx, p = _run_moe(qtype, wg, wu, wd, x, logits, d_model, d_ff, e, k)
+    ridx, rp = oracle.moe_route(logits, k)
+    assert np.array_equal(idx, ridx), "routing differs from the oracle"
+    assert np.allclose(p, rp, rtol=1e-6, atol=0)
+    # expert FFNs only for the routed experts (dequantise what is used)
+    used = sorted(set(ridx.ravel().tolist()))
+    dg = {i: oracle.dequant(qtype, wg[i], d_ff, d_model) for i in used}
+    du = {i: oracle.dequant(qtype, wu[i], d_ff, d_model) for i in used}
+    dd = {i: oracle.dequant(qtype, wd[i], d_model, d_ff) for i in used}
+    ref = np.zeros((t, d_model))
+    tol = np.zeros((t, d_model))
+    for ti in range(t):
+        for j in range(k):
+            ex = int(ridx[ti, j])
+            ye, te, _ = oracle.swiglu_ffn(dg[ex], du[ex], dd[ex], x[ti:ti + 1])
+            ref[ti] += rp[ti, j] * ye[0]
+            tol[ti] += rp[ti, j] * (te[0] + 1e-5 * np.abs(ye[0]) + 1e-6 * np.abs(ye[0]))
+    assert_within(y, ref, tol, f"moe {qtype} T={t} E={e} k={k}")
+    check_device_clean()
+
+
+def test_moe_one_hot_equals_ffn_and_is_deterministic():
+    qtype, t, e, k, d_model, d_ff = "q4_k", 3, 6, 1, 512, 256
+    wg, wu, wd = _experts(qtype, 520, e, d_model, d_ff)
+    x = synth.normal_f32(520, 1, (t, d_model))
+    logits = np.full((t, e), -4.0, dtype=np.float32)
+    chosen = [5, 0, 5]
+    for ti, c in enumerate(chosen):
+        logits[ti, c] = 4.0
+    y, idx, p = _run_moe(qtype, wg, wu, wd, x, logits, d_model, d_ff, e, k)
+    y2, _, _ = _run_moe(qtype, wg, wu, wd, x, logits, d_model, d_ff, e, k)
+    assert np.array_equal(y, y2)
+    assert idx[:, 0].tolist() == chosen and np.all(p == 1.0)
+    for ti, c in enumerate(chosen):
+        yf = to_host(phb.ffn_swiglu(qtype, to_dev(wg[c]), to_dev(wu[c]), to_dev(wd[c]), to_dev(x[ti:ti + 1]),
+                                    d_model, d_ff))
+        ref, tol, _ = oracle.swiglu_ffn(oracle.dequant(qtype, wg[c], d_ff, d_model),
+                                        oracle.dequant(qtype, wu[c], d_ff, d_model),
+                                        oracle.dequant(qtype, wd[c], d_model, d_ff), x[ti:ti + 1])
+        assert_within(y[ti], ref[0], tol[0], "one-hot moe")
+        assert_within(yf[0], ref[0], tol[0], "ffn")
+
+
+def test_moe_all_logits_equal_picks_lowest_experts():
+    qtype, t, e, k, d_model, d_ff = "q4_k", 2, 16, 8, 256, 256
+    wg, wu, wd = _experts(qtype, 530, e, d_model, d_ff)
+    x = synth.normal_f32(530, 1, (t, d_model))
+    logits = np.zeros((t, e), dtype=np.float32)
+    _, idx, p = _run_moe(qtype, wg, wu, wd, x, logits, d_model, d_ff, e, k)
+    assert idx.tolist() == [list(range(8))] * t
+    assert np.allclose(p, 1 / 8, rtol=1e-7)
+
+
+# ---------------------------------------------------------------- decode step
+
+D_MODEL, N_Q, N_KV, HD, D_FF = 2048, 16, 4, 128, 5632
+QKV = (N_Q + 2 * N_KV) * HD
+
+
+def _layer_blobs(qtype, seed, layer):
+    base = 5 * layer
+    return [synth.blocks(qtype, seed, base + 0, QKV, D_MODEL), synth.blocks(qtype, seed, base + 1, D_MODEL, N_Q * HD),
+            synth.blocks(qtype, seed, base + 2, D_FF, D_MODEL), synth.blocks(qtype, seed, base + 3, D_FF, D_MODEL),
+            synth.blocks(qtype, seed, base + 4, D_MODEL, D_FF)]
+
+
+def _deq_layer(qtype, blobs):
+    shapes = [(QKV, D_MODEL), (D_MODEL, N_Q * HD), (D_FF, D_MODEL), (D_FF, D_MODEL), (D_MODEL, D_FF)]
+    return [oracle.dequant(qtype, b, r, c) for b, (r, c) in zip(blobs, shapes)]
+
+
+@pytest.mark.parametrize("qtype", ["q8_0", "q4_k"])
+def test_decode_single_layer_within_bound(qtype):
+    blobs = _layer_blobs(qtype, 600, 0)
+    dev = [to_dev(b) for b in blobs]
+    table = phb.layer_table([dev])
+    x = synth.normal_f32(600, 999, (D_MODEL,))
+    y = to_host(phb.decode_step(qtype, table, 1, D_MODEL, N_Q, N_KV, HD, D_FF, to_dev(x)))
+    ref, bound = oracle.decode_layer(x, np.zeros((1, D_MODEL)), *_deq_layer(qtype, blobs), N_Q, N_KV, HD)
+    assert_within(y[None, :], ref, bound, f"decode layer {qtype}")
+    check_device_clean()
+
+
+def test_decode_24_layers_layerwise_and_composed():
+    """The 24-layer step equals 24 chained single-layer steps bit for bit, and
+    every layer is within its bound of the oracle layer applied to the same
+    (GPU-produced) input. A worst-case bound propagated through 24 random
+    layers grows by orders of magnitude per layer, so each layer is checked
+    from its own input instead (errors do not compound)."""
+    qtype, n_layers = "q8_0", 24
+    seed = synth.workload_seed(1)
+    x = synth.normal_f32(seed, 100_000, (D_MODEL,))
+    blobs = [_layer_blobs(qtype, seed, layer) for layer in range(n_layers)]
+    dev_layers = [[to_dev(b) for b in bl] for bl in blobs]
+    table = phb.layer_table(dev_layers)
+    y = to_host(phb.decode_step(qtype, table, n_layers, D_MODEL, N_Q, N_KV, HD, D_FF, to_dev(x)))
+    cur = x
+    ref_chain = x.astype(np.float64)[None, :]
+    for layer in range(n_layers):
+        one = phb.layer_table([dev_layers[layer]])
+        nxt = to_host(phb.decode_step(qtype, one, 1, D_MODEL, N_Q, N_KV, HD, D_FF, to_dev(cur)))
+        mats = _deq_layer(qtype, blobs[layer])
+        ref, bound = oracle.decode_layer(cur, np.zeros((1, D_MODEL)), *mats, N_Q, N_KV, HD)
+        assert_within(nxt[None, :], ref, bound, f"layer {layer}")
+        ref_chain, _ = oracle.decode_layer(ref_chain, np.zeros((1, D_MODEL)), *mats, N_Q, N_KV, HD)
+        cur = nxt
+    assert np.array_equal(y, cur), "24-layer call differs from 24 chained single-layer calls"
+    # the whole chain also stays close to the all-float64 chain (informative, loose)
+    rel = np.abs(y - ref_chain[0]).max() / np.abs(ref_chain[0]).max()
+    assert rel < 1e-3, rel
+    check_device_clean()
