@@ -297,6 +297,8 @@ phb_status phb_ffn_swiglu(int qtype, const void* Wgate, const void* Wup, const v
         q.nmat = 2;
         q.w1 = Wup;
         q.epi = 2;
+        q.pf[0] = Wdown;  // the down projection streams into L2 while gate/up computes
+        q.pf_bytes[0] = d_model * static_cast<int64_t>(phb_row_bytes(qtype, d_ff));
         st = run_gemv(q, stream);
         if (st != PHB_OK) return st;
     } else {
@@ -455,6 +457,10 @@ phb_status phb_decode_step(int qtype, const phb_dense_layer* layers, int n_layer
     if (st != PHB_OK) return st;
     const DecodeWs w = decode_ws(d_model, n_q_heads, n_kv_heads, head_dim, d_ff, ws);
     const int64_t qkv_dim = static_cast<int64_t>(n_q_heads + 2 * n_kv_heads) * head_dim;
+    // GEMV launch ids for debug tracing builds. (Prefetching the weights of
+    // GEMV i + 2 into L2 from GEMV i measured slightly slower here, so the
+    // decode step issues no prefetch.)
+    auto set_pf = [&](phb::GemvReq& q, int op) { q.trace_id = op; };
     for (int l = 0; l < n_layers; ++l) {
         const phb_dense_layer& L = layers[l];
         const float* in = l == 0 ? x_in : w.xs[(l - 1) & 1];
@@ -462,6 +468,7 @@ phb_status phb_decode_step(int qtype, const phb_dense_layer* layers, int n_layer
         // QKV = Wqkv . rmsnorm(x)
         phb::GemvReq q = gemv_req(qt, L.w_qkv, in, w.qkv, qkv_dim, d_model, 1);
         q.xmode = 1;
+        set_pf(q, 4 * l);
         PHB_CUDA(phb::decode_gemv_run(q, stream), "decode qkv launch");
         // x1 = x + Wo . attn(qkv)
         q = gemv_req(qt, L.w_o, w.qkv, w.x1, d_model, q_dim, 1);
@@ -471,6 +478,7 @@ phb_status phb_decode_step(int qtype, const phb_dense_layer* layers, int n_layer
         q.gather_group = n_q_heads / n_kv_heads;
         q.gather_hd = head_dim;
         q.gather_v_off = static_cast<int64_t>(n_q_heads + n_kv_heads) * head_dim;
+        set_pf(q, 4 * l + 1);
         PHB_CUDA(phb::decode_gemv_run(q, stream), "decode o launch");
         // act = silu(Wg . rmsnorm(x1)) * (Wu . rmsnorm(x1))
         q = gemv_req(qt, L.w_gate, w.x1, w.act, d_ff, d_model, 1);
@@ -478,11 +486,13 @@ phb_status phb_decode_step(int qtype, const phb_dense_layer* layers, int n_layer
         q.w1 = L.w_up;
         q.xmode = 1;
         q.epi = 2;
+        set_pf(q, 4 * l + 2);
         PHB_CUDA(phb::decode_gemv_run(q, stream), "decode gate/up launch");
         // out = x1 + Wd . act
         q = gemv_req(qt, L.w_down, w.act, out, d_model, d_ff, 1);
         q.epi = 1;
         q.r = w.x1;
+        set_pf(q, 4 * l + 3);
         PHB_CUDA(phb::decode_gemv_run(q, stream), "decode down launch");
     }
     return ok();

@@ -38,6 +38,8 @@ __device__ __forceinline__ float2 ffma2(float a0, float a1, float b0, float b1, 
     return __ffma2_rn(make_float2(a0, a1), make_float2(b0, b1), c);
 }
 
+// Rows b >= batch of the staged activations are zero, so the loops below run
+// over all MAXB rows without guards.
 // Activation layout in shared memory: a pad of 4 floats after every 128, so
 // consecutive half units start in different bank groups.
 constexpr int kXPadEvery = 128;
@@ -52,7 +54,7 @@ __device__ __forceinline__ int xpad_idx(int k) { return k + (k / kXPadEvery) * k
 //   xfac: per-row 2^(149 - s)
 template <int MAXB>
 __device__ __forceinline__ void dot_q8_0_half(const uint8_t* wsrc, const float* xs, int xstride, const float* xsum,
-                                              int sstride, const float* xfac, int batch, float (&acc)[MAXB]) {
+                                              int sstride, const float* xfac, float (&acc)[MAXB]) {
     uint32_t wd[34];
 #pragma unroll
     for (int i = 0; i < 17; ++i) {
@@ -80,20 +82,16 @@ __device__ __forceinline__ void dot_q8_0_half(const uint8_t* wsrc, const float* 
             }
 #pragma unroll
             for (int b = 0; b < MAXB; ++b) {
-                if (b < batch) {
-                    const float4 xv = *reinterpret_cast<const float4*>(xs + b * xstride + 32 * bb + 4 * i4);
-                    s2[b] = ffma2(q[0], q[1], xv.x, xv.y, s2[b]);
-                    s2[b] = ffma2(q[2], q[3], xv.z, xv.w, s2[b]);
-                }
+                const float4 xv = *reinterpret_cast<const float4*>(xs + b * xstride + 32 * bb + 4 * i4);
+                s2[b] = ffma2(q[0], q[1], xv.x, xv.y, s2[b]);
+                s2[b] = ffma2(q[2], q[3], xv.z, xv.w, s2[b]);
             }
         }
 #pragma unroll
         for (int b = 0; b < MAXB; ++b) {
-            if (b < batch) {
-                const float su = s2[b].x + s2[b].y;
-                const float blk = fmaf(su, xfac[b], -128.f * xsum[b * sstride + bb]);
-                acc[b] = fmaf(d, blk, acc[b]);
-            }
+            const float su = s2[b].x + s2[b].y;
+            const float blk = fmaf(su, xfac[b], -128.f * xsum[b * sstride + bb]);
+            acc[b] = fmaf(d, blk, acc[b]);
         }
     }
 }
@@ -119,8 +117,7 @@ __device__ __forceinline__ void q4_k_scale_min(const uint32_t (&sw)[3], int j, u
 //   xs, xsum, xfac: as for Q8_0 (xsum points at sub-block 4h of the block)
 template <int MAXB>
 __device__ __forceinline__ void dot_q4_k_half(const uint8_t* blk, int h, const float* xs, int xstride,
-                                              const float* xsum, int sstride, const float* xfac, int batch,
-                                              float (&acc)[MAXB]) {
+                                              const float* xsum, int sstride, const float* xfac, float (&acc)[MAXB]) {
     const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
     const float d = fp16_bits_to_float(hdr.x);
     const float dmin = fp16_bits_to_float(hdr.x >> 16);
@@ -150,14 +147,12 @@ __device__ __forceinline__ void dot_q4_k_half(const uint8_t* blk, int h, const f
             const float h2 = byte_subnormal<2>(hi), h3 = byte_subnormal<3>(hi);
 #pragma unroll
             for (int b = 0; b < MAXB; ++b) {
-                if (b < batch) {
-                    const float4 xl = *reinterpret_cast<const float4*>(xs + b * xstride + 64 * cc + 4 * wi);
-                    const float4 xh = *reinterpret_cast<const float4*>(xs + b * xstride + 64 * cc + 32 + 4 * wi);
-                    slo[b] = ffma2(l0, l1, xl.x, xl.y, slo[b]);
-                    slo[b] = ffma2(l2, l3, xl.z, xl.w, slo[b]);
-                    shi[b] = ffma2(h0, h1, xh.x, xh.y, shi[b]);
-                    shi[b] = ffma2(h2, h3, xh.z, xh.w, shi[b]);
-                }
+                const float4 xl = *reinterpret_cast<const float4*>(xs + b * xstride + 64 * cc + 4 * wi);
+                const float4 xh = *reinterpret_cast<const float4*>(xs + b * xstride + 64 * cc + 32 + 4 * wi);
+                slo[b] = ffma2(l0, l1, xl.x, xl.y, slo[b]);
+                slo[b] = ffma2(l2, l3, xl.z, xl.w, slo[b]);
+                shi[b] = ffma2(h0, h1, xh.x, xh.y, shi[b]);
+                shi[b] = ffma2(h2, h3, xh.z, xh.w, shi[b]);
             }
         }
         uint32_t sc_l, m_l, sc_h, m_h;
@@ -167,14 +162,12 @@ __device__ __forceinline__ void dot_q4_k_half(const uint8_t* blk, int h, const f
         const float dh = d * static_cast<float>(sc_h), mh = dmin * static_cast<float>(m_h);
 #pragma unroll
         for (int b = 0; b < MAXB; ++b) {
-            if (b < batch) {
-                const float ql = (slo[b].x + slo[b].y) * xfac[b];
-                const float qh = (shi[b].x + shi[b].y) * xfac[b];
-                acc[b] = fmaf(dl, ql, acc[b]);
-                acc[b] = fmaf(-ml, xsum[b * sstride + 2 * cc], acc[b]);
-                acc[b] = fmaf(dh, qh, acc[b]);
-                acc[b] = fmaf(-mh, xsum[b * sstride + 2 * cc + 1], acc[b]);
-            }
+            const float ql = (slo[b].x + slo[b].y) * xfac[b];
+            const float qh = (shi[b].x + shi[b].y) * xfac[b];
+            acc[b] = fmaf(dl, ql, acc[b]);
+            acc[b] = fmaf(-ml, xsum[b * sstride + 2 * cc], acc[b]);
+            acc[b] = fmaf(dh, qh, acc[b]);
+            acc[b] = fmaf(-mh, xsum[b * sstride + 2 * cc + 1], acc[b]);
         }
     }
 }

@@ -1,19 +1,29 @@
 // Streaming dequantize-GEMV building blocks for sm_103a.
 //
 // A CTA owns a tile: rows [row0, row0 + rows_here) of each of its NMAT
-// matrices, restricted to the K slice of units [u0, u0 + useg). The tile's
-// weight bytes are a list of 256-weight units (272 B of Q8_0, 144 B of Q4_K),
-// ordered matrix-major, then row, then unit. One producer thread streams the
-// list into a ring of shared-memory stages with 1-D bulk copies (the TMA
-// engine) that complete on mbarriers. Eight consumer warps dequantise one
-// half unit per thread per stage in registers and dot it with activations
-// staged in shared memory (gemv_core.cuh). After each stage the half-unit
-// sums of every row the stage touched are added, in unit order, to that
-// row's accumulator; accumulation order is therefore fixed and results are
-// bitwise reproducible.
+// matrices (NMAT = 2 for the fused gate/up pair), restricted to the K slice
+// of units [u0, u0 + useg). The tile's weight bytes are a list of 256-weight
+// units (272 B of Q8_0, 144 B of Q4_K) ordered by row, then matrix, then
+// unit, so row r of the gate matrix is followed by row r of the up matrix.
+// One producer thread streams the list into a ring of shared-memory stages
+// with 1-D bulk copies (the TMA engine) that complete on mbarriers; it also
+// prefetches into L2 a share of the weights the next kernels will read, so
+// HBM keeps streaming across kernel boundaries. CW consumer warps dequantise
+// one half unit (128 weights) per thread per stage in registers and dot it
+// with activations staged in shared memory (gemv_core.cuh). Thread t owns
+// half unit t of a stage, so a warp holds 32 consecutive half units.
 //
-// The dense kernel (gemv_stream_kernel) issues its weight copies before the
-// programmatic-dependent-launch wait, so they overlap the previous kernel.
+// Row sums, three ways, all in a fixed order (bitwise reproducible):
+//  - warp rows: when a row segment (a gate/up pair counting as one) is a
+//    power of two of at most 32 half units, every warp holds whole rows,
+//    reduced by a butterfly of warp shuffles; the lane that owns a row runs
+//    the epilogue at once and no block barrier is needed;
+//  - tile partials: otherwise, when the tile's half-unit sums fit, they stay
+//    in shared memory and after the last stage one warp per row reduces
+//    them (lanes strided over the row, then a butterfly);
+//  - stage fold: otherwise each stage's sums are added, in unit order, to
+//    per-row accumulators after the stage.
+//
 // Every mbarrier wait is bounded (kSpinLimit); one that runs out sets the
 // translation unit's device error word and the kernel returns.
 #pragma once
@@ -26,22 +36,49 @@ namespace phb {
 // Device error word of the translation unit that includes this header.
 static __device__ int g_dev_err;
 
+#ifdef PHB_TRACE
+// Debug builds only: per-CTA timestamps [launch id][cta][event].
+constexpr int kTraceLaunches = 128, kTraceCtas = 160, kTraceEvents = 6;
+static __device__ uint64_t g_trace[kTraceLaunches * kTraceCtas * kTraceEvents];
+#define PHB_TRACE_EV(id, ev)                                                                          \
+    do {                                                                                              \
+        if ((id) >= 0 && (id) < kTraceLaunches && blockIdx.x < kTraceCtas && blockIdx.y == 0)          \
+            g_trace[((id) * kTraceCtas + blockIdx.x) * kTraceEvents + (ev)] = global_timer_ns();        \
+    } while (0)
+#else
+#define PHB_TRACE_EV(id, ev) \
+    do {                     \
+    } while (0)
+#endif
+
 enum XMode : int { kXPlain = 0, kXRmsNorm = 1, kXGatherV = 2, kXRowList = 3 };
 enum Epi : int { kEpiStore = 0, kEpiResid = 1, kEpiSwiGLU = 2 };
+enum RowSum : int { kSumWarp = 0, kSumTile = 1, kSumFold = 2 };
 
-constexpr int kConsumerWarps = 8;
-constexpr int kConsumers = 32 * kConsumerWarps;
-constexpr int kGemvThreads = kConsumers + 32;
-constexpr int kStageUnits = 128;   // 256 half units: one per consumer thread
-constexpr int kAccStride = 8;      // floats per (half unit | row) accumulator slot
+constexpr int kAccStride = 8;      // floats per row accumulator slot (max batch)
 constexpr float kRmsEps = 1e-6f;
+constexpr int kMaxConsumerWarps = 16;
 
-template <int QT> struct StageCfg;
-template <> struct StageCfg<0> { static constexpr int ns = 2; };  // 2 x 34816 B
-template <> struct StageCfg<1> { static constexpr int ns = 4; };  // 4 x 18432 B
+// Per-configuration constants: QT format, CW consumer warps.
+template <int QT, int CW>
+struct KCfg {
+    static constexpr int consumers = 32 * CW;
+    static constexpr int threads = consumers + 32;    // + one producer warp
+    static constexpr int stage_units = consumers / 2; // one half unit per consumer thread
+    static constexpr int ub = Fmt<QT>::unit_bytes;
+    static constexpr int stage_bytes = stage_units * ub;
+    // ring depth: 70 KB of Q8_0 or 55 KB of Q4_K at 8 warps, so that two
+    // CTAs (this kernel's and the next one's) fit on an SM
+    static constexpr int ns = QT == 0 ? 2 : 3;
+};
 
+// Floats after the mbarriers: xfac [kAccStride], reduction scratch
+// [(2 * kMaxConsumerWarps + 3) * kAccStride], row list [kAccStride] (ints).
+constexpr int kTailFloats = kAccStride * (1 + 2 * kMaxConsumerWarps + 3 + 1);
+
+template <int N>
 __device__ __forceinline__ void consumer_sync() {
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+    asm volatile("bar.sync 1, %0;" ::"n"(N) : "memory");
 }
 
 // Geometry of one CTA tile.
@@ -53,234 +90,325 @@ struct Tile {
     bool contiguous;       // useg covers whole rows (consecutive rows adjacent)
 };
 
-__device__ __forceinline__ int tile_units(const Tile& t, int nmat) { return nmat * t.rows_here * t.useg; }
+// True when rows reduce inside a warp (see the header comment).
+__host__ __device__ __forceinline__ bool warp_rows(int useg, int nmat) {
+    const int seg = 2 * useg * nmat;
+    return seg <= 32 && (seg & (seg - 1)) == 0;
+}
 
-// Producer: stream `nst` stages of the tile's unit list, continuing the ring
-// position `s` (stage counter shared with the consumers). Returns false on a
-// wait timeout.
-template <int QT>
+// Prefetch this CTA's share of [p, p + bytes) into L2 (fire and forget).
+__device__ __forceinline__ void prefetch_share(const uint8_t* p, int64_t bytes) {
+    if (p == nullptr || bytes <= 0) return;
+    const int64_t chunk = ((bytes + gridDim.x * gridDim.y - 1) / (gridDim.x * gridDim.y) + 15) & ~int64_t{15};
+    const int64_t cta = static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x;
+    int64_t lo = cta * chunk;
+    const int64_t hi = min(bytes, lo + chunk) & ~int64_t{15};
+    lo &= ~int64_t{15};
+    constexpr int64_t kPiece = 32768;
+    for (; lo < hi; lo += kPiece) prefetch_l2(p + lo, static_cast<uint32_t>(min(kPiece, hi - lo)));
+}
+
+// Producer: stream the tile's unit list through the stage ring, continuing
+// the ring position `s` (a stage counter shared with the consumers).
+// Returns false on a wait timeout.
+template <int QT, int CW>
 __device__ __forceinline__ bool produce_tile(const Tile& t, int nmat, uint8_t* stages, uint64_t* full,
                                              uint64_t* empty, int& s, uint64_t pol) {
-    constexpr int UB = Fmt<QT>::unit_bytes;
-    constexpr int NS = StageCfg<QT>::ns;
-    constexpr int SB = kStageUnits * UB;
-    const int units_mat = t.rows_here * t.useg;
-    const int units = nmat * units_mat;
-    for (int g0 = 0; g0 < units; g0 += kStageUnits, ++s) {
-        const int slot = s % NS;
-        if (s >= NS && !mbar_wait(&empty[slot], ((s / NS) - 1) & 1, &g_dev_err)) return false;
-        const int g1 = min(units, g0 + kStageUnits);
-        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>((g1 - g0) * UB));
-        uint8_t* dst = stages + slot * SB;
+    using C = KCfg<QT, CW>;
+    const int units = nmat * t.rows_here * t.useg;
+    // with one matrix and whole rows the list is one contiguous byte range
+    const bool flat = (nmat == 1) && t.contiguous;
+    for (int g0 = 0; g0 < units; g0 += C::stage_units, ++s) {
+        const int slot = s % C::ns;
+        if (s >= C::ns && !mbar_wait(&empty[slot], ((s / C::ns) - 1) & 1, &g_dev_err)) return false;
+        const int g1 = min(units, g0 + C::stage_units);
+        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>((g1 - g0) * C::ub));
+        uint8_t* dst = stages + slot * C::stage_bytes;
+        if (flat) {
+            bulk_g2s_hint(dst, t.w[0] + static_cast<int64_t>(g0) * C::ub, static_cast<uint32_t>((g1 - g0) * C::ub),
+                          &full[slot], pol);
+            continue;
+        }
         int g = g0;
         while (g < g1) {
-            const int mat = g / units_mat;
-            const int rem = g - mat * units_mat;
-            const int r = rem / t.useg;
-            const int u = rem - r * t.useg;
-            const int end = t.contiguous ? min(g1, (mat + 1) * units_mat) : min(g1, g + (t.useg - u));
-            const uint8_t* src = (mat == 0 ? t.w[0] : t.w[1]) + r * t.row_bytes + static_cast<int64_t>(u) * UB;
-            bulk_g2s_hint(dst + (g - g0) * UB, src, static_cast<uint32_t>((end - g) * UB), &full[slot], pol);
+            const int seg = g / t.useg;       // row * nmat + mat
+            const int u = g - seg * t.useg;
+            const int r = seg / nmat;
+            const int mat = seg - r * nmat;
+            const int end = min(g1, g + (t.useg - u));
+            const uint8_t* src = (mat == 0 ? t.w[0] : t.w[1]) + r * t.row_bytes + static_cast<int64_t>(u) * C::ub;
+            bulk_g2s_hint(dst + (g - g0) * C::ub, src, static_cast<uint32_t>((end - g) * C::ub), &full[slot], pol);
             g = end;
         }
     }
     return true;
 }
 
-// Consumers: dot every staged half unit with the activations and fold the
-// sums into row_acc[(mat * rows_here + r) * kAccStride + b]. row_acc must be
-// zeroed by the caller. Consumer thread t owns half unit t of each stage
-// (unit t/2, half t%2), so a warp reads 32 consecutive half units: bank
-// conflict free for the weights, and (with the padded activation layout)
-// for the activations. Returns false on a wait timeout.
-//   xs, xsum, xfac: staged activations (see stage_x)
-template <int QT, int MAXB>
-__device__ __forceinline__ bool consume_tile(const Tile& t, int nmat, const uint8_t* stages, uint64_t* full,
+// Consumers: dot every staged half unit with the activations and hand each
+// finished row to epi(r, b, a0, a1) for b < batch, with a0 the row's sum
+// (the gate row's for NMAT == 2) and a1 the up row's sum. `mode` is the
+// row-sum method (kSumWarp needs warp_rows). `part` holds
+// 2 * units * MAXB floats for kSumTile, MAXB * consumers for kSumFold;
+// `row_acc` NMAT * rows_here * kAccStride floats (kSumFold; zeroed by the
+// caller before its last consumer barrier). Returns false on a wait timeout.
+template <int QT, int CW, int MAXB, int NMAT, class EpiF>
+__device__ __forceinline__ bool consume_tile(const Tile& t, int mode, const uint8_t* stages, uint64_t* full,
                                              uint64_t* empty, int& s, const float* xs, int xstride,
                                              const float* xsum, int sstride, const float* xfac, int batch,
-                                             float* part, float* row_acc) {
-    constexpr int UB = Fmt<QT>::unit_bytes;
-    constexpr int NS = StageCfg<QT>::ns;
-    constexpr int SB = kStageUnits * UB;
+                                             float* part, float* row_acc, EpiF epi) {
+    using C = KCfg<QT, CW>;
     const int tid = threadIdx.x;
-    const int lane = tid & 31;
+    const int warp = tid >> 5, lane = tid & 31;
     const int hsel = tid & 1;
     const int ulocal = tid >> 1;
-    const int units = nmat * t.rows_here * t.useg;
-    for (int g0 = 0; g0 < units; g0 += kStageUnits, ++s) {
-        const int slot = s % NS;
-        if (!mbar_wait(&full[slot], (s / NS) & 1, &g_dev_err)) {
-            mbar_wait(&full[slot], (s / NS) & 1, &g_dev_err);  // second bounded wait for the copy in flight
+    const int units = NMAT * t.rows_here * t.useg;
+    const int seg_half = 2 * t.useg;  // half units per row segment
+    for (int g0 = 0; g0 < units; g0 += C::stage_units, ++s) {
+        const int slot = s % C::ns;
+        if (!mbar_wait_warp(&full[slot], (s / C::ns) & 1, &g_dev_err)) {
+            mbar_wait(&full[slot], (s / C::ns) & 1, &g_dev_err);  // second bounded wait for the copy in flight
             return false;
         }
         const int g = g0 + ulocal;
+        const int segi = g / t.useg;
+        const int u = g - segi * t.useg;
         float acc[MAXB];
 #pragma unroll
         for (int b = 0; b < MAXB; ++b) acc[b] = 0.f;
         if (g < units) {
-            const int hu = 2 * (g % t.useg) + hsel;  // half unit within the row segment
-            const uint8_t* ub = stages + slot * SB + ulocal * UB;
+            const int hu = 2 * u + hsel;  // half unit within the row segment
+            const uint8_t* ub = stages + slot * C::stage_bytes + ulocal * C::ub;
             const float* xsp = xs + hu * (kXPadEvery + kXPad);
             const float* xsm = xsum + hu * 4;
             if constexpr (QT == 0)
-                dot_q8_0_half<MAXB>(ub + 136 * hsel, xsp, xstride, xsm, sstride, xfac, batch, acc);
+                dot_q8_0_half<MAXB>(ub + 136 * hsel, xsp, xstride, xsm, sstride, xfac, acc);
             else
-                dot_q4_k_half<MAXB>(ub, hsel, xsp, xstride, xsm, sstride, xfac, batch, acc);
+                dot_q4_k_half<MAXB>(ub, hsel, xsp, xstride, xsm, sstride, xfac, acc);
+        }
+        if (mode == kSumWarp) {
+            float other[MAXB];
+#pragma unroll
+            for (int b = 0; b < MAXB; ++b) {
+                float v = acc[b];
+                for (int o = 1; o < seg_half; o <<= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+                acc[b] = v;
+                other[b] = NMAT == 2 ? __shfl_xor_sync(0xFFFFFFFFu, v, seg_half) : 0.f;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+            if ((lane & (NMAT * seg_half - 1)) == 0 && g < units) {
+                const int r = segi / NMAT;
+#pragma unroll
+                for (int b = 0; b < MAXB; ++b)
+                    if (b < batch) epi(r, b, acc[b], other[b]);
+            }
+            continue;
+        }
+        if (mode == kSumTile) {
+            if (g < units) {
+#pragma unroll
+                for (int b = 0; b < MAXB; ++b) part[(2 * g + hsel) * MAXB + b] = acc[b];
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+            continue;
         }
 #pragma unroll
-        for (int b = 0; b < MAXB; ++b) part[b * 2 * kStageUnits + tid] = acc[b];
+        for (int b = 0; b < MAXB; ++b) part[b * C::consumers + tid] = acc[b];
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
-        consumer_sync();
-        // fold this stage into the rows it touched, half units in order
-        const int g1 = min(units, g0 + kStageUnits);
+        consumer_sync<C::consumers>();
+        // fold this stage into the row segments it touched, half units in order
+        const int g1 = min(units, g0 + C::stage_units);
         const int r_first = g0 / t.useg, r_last = (g1 - 1) / t.useg;
         const int items = (r_last - r_first + 1) * batch;
-        for (int it = tid; it < items; it += kConsumers) {
+        for (int it = tid; it < items; it += C::consumers) {
             const int rr = r_first + it / batch;
             const int b = it - (it / batch) * batch;
             const int ha = 2 * (max(g0, rr * t.useg) - g0), hb = 2 * (min(g1, (rr + 1) * t.useg) - g0);
-            const float* q = part + b * 2 * kStageUnits;
+            const float* q = part + b * C::consumers;
             float sum = row_acc[rr * kAccStride + b];
             for (int hh = ha; hh < hb; ++hh) sum += q[hh];
             row_acc[rr * kAccStride + b] = sum;
         }
-        consumer_sync();
+        consumer_sync<C::consumers>();
+    }
+    if (mode == kSumTile) {
+        consumer_sync<C::consumers>();
+        // one warp per row: lanes strided over the row's half units, then a butterfly
+        for (int r = warp; r < t.rows_here; r += CW) {
+            float a[NMAT][MAXB];
+#pragma unroll
+            for (int m = 0; m < NMAT; ++m) {
+                const float* base = part + static_cast<size_t>(r * NMAT + m) * seg_half * MAXB;
+#pragma unroll
+                for (int b = 0; b < MAXB; ++b) {
+                    float v = 0.f;
+                    for (int j = lane; j < seg_half; j += 32) v += base[j * MAXB + b];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+                    a[m][b] = v;
+                }
+            }
+            if (lane == 0) {
+#pragma unroll
+                for (int b = 0; b < MAXB; ++b)
+                    if (b < batch) epi(r, b, a[0][b], a[NMAT - 1][b]);
+            }
+        }
+    } else if (mode == kSumFold) {
+        for (int it = tid; it < t.rows_here * batch; it += C::consumers) {
+            const int r = it / batch;
+            const int b = it - r * batch;
+            const float a0 = row_acc[(r * NMAT) * kAccStride + b];
+            const float a1 = NMAT == 2 ? row_acc[(r * NMAT + 1) * kAccStride + b] : 0.f;
+            epi(r, b, a0, a1);
+        }
     }
     return true;
 }
 
 // Stage activations a[b][0 .. kseg) for b < batch into shared memory:
-//   xs   [b][xpad_len(kseg)]: a * 2^s_b in the padded layout (xpad_idx)
-//   xsum [b][kseg/32]:        unscaled sums of every 32 consecutive a
-//   xfac [b]:                 2^(149 - s_b)
-// a is x[b][kbase + k] (kXPlain), x[rowidx[b]][k] (kXRowList), rmsnorm of
-// the whole row (kXRmsNorm), or the V head of the query head that owns k
-// (kXGatherV). s_b is chosen from
-// max|a| so that |a| * 2^s_b < 2^125. `red` needs (kConsumerWarps+1) *
-// kAccStride floats. Ends with a consumer barrier.
+//   xs   [MAXB][xpad_len(kseg)]: a * 2^s_b in the padded layout (xpad_idx)
+//   xsum [MAXB][kseg/32]:        sums of every 32 consecutive a
+//   xfac [MAXB]:                 2^(149 - s_b)
+// Rows batch..MAXB-1 are zero (xfac 1). a is x[b][kbase + k] (kXPlain),
+// x[rowidx[b]][k] (kXRowList), the V head of the query head that owns k
+// (kXGatherV), or x[b][k] * r_b with r_b = (mean_k x^2 + eps)^-1/2
+// (kXRmsNorm; rows are whole). s_b is chosen from max|a| so that
+// |a| * 2^s_b < 2^125. One global read pass, three consumer barriers.
+// `red` needs (2 * CW + 3) * kAccStride floats.
 __device__ __forceinline__ int pick_scale_exp(float amax) {
     if (!(amax > 0.f) || !isfinite(amax)) return 125;
     const int e = ilogbf(amax) + 1;  // amax < 2^e
     return min(270, max(22, 125 - e));
 }
 
-template <int QT, int MAXB, int XMODE>
+template <int CW, int MAXB, int XMODE>
 __device__ __forceinline__ void stage_x(const float* x, int64_t ldx, int64_t kbase, int kseg, int batch, float* xs,
                                        float* xsum, float* xfac, float* red, int gather_group, int gather_hd,
                                        int64_t gather_v_off, const int* rowidx = nullptr) {
+    constexpr int NC = 32 * CW;
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int xstride = xpad_len(kseg);
-    const int per_row4 = kseg / 4;
-    if constexpr (XMODE == kXGatherV) {
-        for (int i = tid; i < batch * kseg; i += kConsumers) {
-            const int b = i / kseg;
-            const int k = i - b * kseg;
-            const int hh = k / gather_hd;
-            const int e = k - hh * gather_hd;
-            xs[b * xstride + xpad_idx(k)] =
-                x[b * ldx + gather_v_off + static_cast<int64_t>(hh / gather_group) * gather_hd + e];
-        }
-    } else {
-        float ss[MAXB];
+    const int nch = kseg / 8;  // 8-float chunks per row; kseg % 32 == 0, so groups of 4 chunks make a 32-sum
+    const int nsub = kseg / 32;
+    float ssq[MAXB], mx[MAXB];
 #pragma unroll
-        for (int b = 0; b < MAXB; ++b) ss[b] = 0.f;
-        for (int i = tid; i < batch * per_row4; i += kConsumers) {
-            const int b = i / per_row4;
-            const int k4 = i - b * per_row4;
-            const float* src = XMODE == kXRowList ? x + static_cast<int64_t>(rowidx[b]) * ldx : x + b * ldx + kbase;
-            const float4 v = *reinterpret_cast<const float4*>(src + 4 * k4);
-            *reinterpret_cast<float4*>(xs + b * xstride + xpad_idx(4 * k4)) = v;
-            if constexpr (XMODE == kXRmsNorm) {
+    for (int b = 0; b < MAXB; ++b) ssq[b] = mx[b] = 0.f;
+    for (int i = tid; i < MAXB * nch; i += NC) {
+        const int b = i / nch;
+        const int c = i - b * nch;
+        float v[8];
+        if (b < batch) {
+            if constexpr (XMODE == kXGatherV) {
 #pragma unroll
-                for (int bb = 0; bb < MAXB; ++bb) {
-                    if (bb == b) {
-                        ss[bb] = fmaf(v.x, v.x, ss[bb]);
-                        ss[bb] = fmaf(v.y, v.y, ss[bb]);
-                        ss[bb] = fmaf(v.z, v.z, ss[bb]);
-                        ss[bb] = fmaf(v.w, v.w, ss[bb]);
-                    }
+                for (int e = 0; e < 8; ++e) {
+                    const int k = 8 * c + e;
+                    const int hh = k / gather_hd;
+                    v[e] = x[b * ldx + gather_v_off + static_cast<int64_t>(hh / gather_group) * gather_hd +
+                             (k - hh * gather_hd)];
                 }
+            } else {
+                const float* src = XMODE == kXRowList ? x + static_cast<int64_t>(rowidx[b]) * ldx + 8 * c
+                                                      : x + b * ldx + kbase + 8 * c;
+                const float4 p0 = *reinterpret_cast<const float4*>(src);
+                const float4 p1 = *reinterpret_cast<const float4*>(src + 4);
+                v[0] = p0.x;
+                v[1] = p0.y;
+                v[2] = p0.z;
+                v[3] = p0.w;
+                v[4] = p1.x;
+                v[5] = p1.y;
+                v[6] = p1.z;
+                v[7] = p1.w;
             }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = 0.f;
         }
+        float* dst = xs + b * xstride + xpad_idx(8 * c);
+        *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+        *reinterpret_cast<float4*>(dst + 4) = make_float4(v[4], v[5], v[6], v[7]);
+        float cs = ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
+        const float cm = fmaxf(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))),
+                               fmaxf(fmaxf(fabsf(v[4]), fabsf(v[5])), fmaxf(fabsf(v[6]), fabsf(v[7]))));
+        float cq = 0.f;
         if constexpr (XMODE == kXRmsNorm) {
 #pragma unroll
-            for (int b = 0; b < MAXB; ++b) {
-                const float w = warp_sum(ss[b]);
-                if (lane == 0) red[warp * kAccStride + b] = w;
-            }
-            consumer_sync();
-            if (tid < batch) {
-                float tsum = 0.f;
-                for (int w = 0; w < kConsumerWarps; ++w) tsum += red[w * kAccStride + tid];
-                red[kConsumerWarps * kAccStride + tid] = rsqrtf(tsum / static_cast<float>(kseg) + kRmsEps);
-            }
-            consumer_sync();
-            for (int i = tid; i < batch * per_row4; i += kConsumers) {
-                const int b = i / per_row4;
-                const int k4 = i - b * per_row4;
-                const float sc = red[kConsumerWarps * kAccStride + b];
-                float4* p = reinterpret_cast<float4*>(xs + b * xstride + xpad_idx(4 * k4));
-                float4 v = *p;
-                v.x *= sc;
-                v.y *= sc;
-                v.z *= sc;
-                v.w *= sc;
-                *p = v;
+            for (int e = 0; e < 8; ++e) cq = fmaf(v[e], v[e], cq);
+        }
+        // 32-sum over the 4 consecutive lanes holding one 32-weight block
+        const unsigned gmask = 0xFu << (lane & 28);
+        cs += __shfl_xor_sync(gmask, cs, 1);
+        cs += __shfl_xor_sync(gmask, cs, 2);
+        if ((lane & 3) == 0) xsum[b * nsub + (c >> 2)] = cs;
+#pragma unroll
+        for (int bb = 0; bb < MAXB; ++bb) {
+            if (bb == b) {
+                mx[bb] = fmaxf(mx[bb], cm);
+                ssq[bb] += cq;
             }
         }
-    }
-    consumer_sync();
-    // 32-sums and per-row max |a|
-    const int nsub = kseg / 32;
-    float mx[MAXB];
-#pragma unroll
-    for (int b = 0; b < MAXB; ++b) mx[b] = 0.f;
-    for (int i = tid; i < batch * nsub; i += kConsumers) {
-        const int b = i / nsub;
-        const int j = i - b * nsub;
-        const float* src = xs + b * xstride + xpad_idx(32 * j);
-        float tsum = 0.f, tmax = 0.f;
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-            tsum += src[e];
-            tmax = fmaxf(tmax, fabsf(src[e]));
-        }
-        xsum[i] = tsum;
-#pragma unroll
-        for (int bb = 0; bb < MAXB; ++bb)
-            if (bb == b) mx[bb] = fmaxf(mx[bb], tmax);
     }
 #pragma unroll
     for (int b = 0; b < MAXB; ++b) {
-        float v = mx[b];
+        float m = mx[b], q = ssq[b];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-        if (lane == 0) red[warp * kAccStride + b] = v;
+        for (int o = 16; o > 0; o >>= 1) {
+            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+            q += __shfl_xor_sync(0xFFFFFFFFu, q, o);
+        }
+        if (lane == 0) {
+            red[warp * kAccStride + b] = m;
+            red[(CW + warp) * kAccStride + b] = q;
+        }
     }
-    consumer_sync();
-    if (tid < batch) {
-        float v = 0.f;
-        for (int w = 0; w < kConsumerWarps; ++w) v = fmaxf(v, red[w * kAccStride + tid]);
-        const int se = pick_scale_exp(v);
-        red[kConsumerWarps * kAccStride + tid] = static_cast<float>(se);
-        xfac[tid] = ldexpf(1.0f, 149 - se);
+    consumer_sync<NC>();
+    // per row: rms factor r (1 unless kXRmsNorm) and the two power-of-two multipliers
+    float* rfac = red + 2 * CW * kAccStride;  // [MAXB]
+    float* f1 = rfac + kAccStride;             // [MAXB]
+    float* f2 = f1 + kAccStride;               // [MAXB]
+    if (tid < MAXB) {
+        float m = 0.f, q = 0.f;
+        for (int w = 0; w < CW; ++w) {
+            m = fmaxf(m, red[w * kAccStride + tid]);
+            q += red[(CW + w) * kAccStride + tid];
+        }
+        float r = 1.f;
+        if constexpr (XMODE == kXRmsNorm) r = rsqrtf(q / static_cast<float>(kseg) + kRmsEps);
+        const int se = tid < batch ? pick_scale_exp(m * r) : 0;
+        const int e1 = min(se, 127);
+        rfac[tid] = r;
+        f1[tid] = ldexpf(1.0f, e1);
+        f2[tid] = ldexpf(1.0f, se - e1);
+        xfac[tid] = tid < batch ? ldexpf(1.0f, 149 - se) : 1.0f;
     }
-    consumer_sync();
-    for (int i = tid; i < batch * per_row4; i += kConsumers) {
+    consumer_sync<NC>();
+    const int per_row4 = kseg / 4;
+    for (int i = tid; i < batch * per_row4; i += NC) {
         const int b = i / per_row4;
         const int k4 = i - b * per_row4;
-        const int se = static_cast<int>(red[kConsumerWarps * kAccStride + b]);
+        const float r = rfac[b], a = f1[b], c = f2[b];
         float4* p = reinterpret_cast<float4*>(xs + b * xstride + xpad_idx(4 * k4));
         float4 v = *p;
-        v.x = ldexpf(v.x, se);
-        v.y = ldexpf(v.y, se);
-        v.z = ldexpf(v.z, se);
-        v.w = ldexpf(v.w, se);
+        if constexpr (XMODE == kXRmsNorm) {
+            v.x *= r;
+            v.y *= r;
+            v.z *= r;
+            v.w *= r;
+        }
+        v.x = v.x * a * c;
+        v.y = v.y * a * c;
+        v.z = v.z * a * c;
+        v.w = v.w * a * c;
         *p = v;
     }
-    consumer_sync();
+    if constexpr (XMODE == kXRmsNorm) {
+        for (int i = tid; i < batch * nsub; i += NC) xsum[i] *= rfac[i / nsub];
+    }
+    consumer_sync<NC>();
 }
 
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
@@ -296,6 +424,7 @@ struct GemvParams {
     int units_seg;         // units per K split (last split may hold fewer)
     int rows_per_cta;
     int batch;
+    int sum_mode;          // RowSum
     const float* x;
     int64_t ldx;
     float* y;
@@ -306,23 +435,32 @@ struct GemvParams {
     int gather_group;      // kXGatherV: query heads per KV head
     int gather_hd;         // kXGatherV: head dim
     int64_t gather_v_off;  // kXGatherV: offset of V in the qkv vector
+    const uint8_t* pf[2];  // weights of later kernels to prefetch into L2 (optional)
+    int64_t pf_bytes[2];
     uint32_t xs_off, xsum_off, part_off, acc_off, bar_off;  // dynamic shared memory layout
+    int trace_id;          // launch id for debug tracing builds (-1: none)
 };
 
-template <int QT, int MAXB, int NMAT, int XMODE, int EPI>
-__global__ void __launch_bounds__(kGemvThreads, 1) gemv_stream_kernel(const __grid_constant__ GemvParams p) {
+template <int QT, int CW, int MAXB, int NMAT, int XMODE, int EPI>
+__global__ void __launch_bounds__(KCfg<QT, CW>::threads, 1) gemv_stream_kernel(const __grid_constant__ GemvParams p) {
+    using C = KCfg<QT, CW>;
     extern __shared__ __align__(1024) uint8_t smem[];
-    constexpr int NS = StageCfg<QT>::ns;
     float* xs = reinterpret_cast<float*>(smem + p.xs_off);
     float* xsum = reinterpret_cast<float*>(smem + p.xsum_off);
     float* part = reinterpret_cast<float*>(smem + p.part_off);
     float* row_acc = reinterpret_cast<float*>(smem + p.acc_off);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
-    uint64_t* empty = full + NS;
-    float* red = reinterpret_cast<float*>(empty + NS);
-    float* xfac = red + (kConsumerWarps + 1) * kAccStride;
+    uint64_t* empty = full + C::ns;
+    float* xfac = reinterpret_cast<float*>(empty + C::ns);
+    float* red = xfac + kAccStride;
+#ifdef PHB_EXP_XFIRST
+    // experiment: a barrier (in the unused row-list slot) that holds the weight
+    // copies back until the activations are staged
+    uint64_t* xready = reinterpret_cast<uint64_t*>(red + (2 * kMaxConsumerWarps + 3) * kAccStride);
+#endif
 
     const int tid = threadIdx.x;
+    if (tid == 0) PHB_TRACE_EV(p.trace_id, 0);
     const int64_t row0 = static_cast<int64_t>(blockIdx.x) * p.rows_per_cta;
     const int split = blockIdx.y;
     const int u0 = split * p.units_seg;
@@ -331,9 +469,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_stream_kernel(const __gr
     t.useg = min(p.units_seg, p.units_row - u0);
     t.row_bytes = p.row_bytes;
     t.contiguous = (t.useg == p.units_row);
-    constexpr int UB = Fmt<QT>::unit_bytes;
-    t.w[0] = p.w[0] + row0 * p.row_bytes + static_cast<int64_t>(u0) * UB;
-    t.w[1] = p.w[NMAT - 1] + row0 * p.row_bytes + static_cast<int64_t>(u0) * UB;
+    t.w[0] = p.w[0] + row0 * p.row_bytes + static_cast<int64_t>(u0) * C::ub;
+    t.w[1] = p.w[NMAT - 1] + row0 * p.row_bytes + static_cast<int64_t>(u0) * C::ub;
     pdl_launch_dependents();
     if (t.rows_here <= 0 || t.useg <= 0) {
         pdl_wait();
@@ -343,53 +480,74 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_stream_kernel(const __gr
     const int batch = p.batch;
 
     if (tid == 0) {
-        for (int s = 0; s < NS; ++s) {
+        for (int s = 0; s < C::ns; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumerWarps);
+            mbar_init(&empty[s], CW);
         }
+#ifdef PHB_EXP_XFIRST
+        mbar_init(xready, 1);
+#endif
         fence_barrier_init();
     }
-    for (int i = tid; i < NMAT * t.rows_here * kAccStride; i += kGemvThreads) row_acc[i] = 0.f;
+    if (p.sum_mode == kSumFold)
+        for (int i = tid; i < NMAT * t.rows_here * kAccStride; i += C::threads) row_acc[i] = 0.f;
     __syncthreads();
 
-    if (tid >= kConsumers) {
-        if (tid == kConsumers) {
+    if (tid >= C::consumers) {
+        if (tid == C::consumers) {
             int s = 0;
-            produce_tile<QT>(t, NMAT, smem, full, empty, s, policy_evict_first());
+            const uint64_t pol = policy_evict_first();
+#ifdef PHB_EXP_XFIRST
+            mbar_wait(xready, 0, &g_dev_err);
+#endif
+            produce_tile<QT, CW>(t, NMAT, smem, full, empty, s, pol);
+        } else if (tid == C::consumers + 1) {
+#ifndef PHB_NO_L2PF
+            prefetch_share(p.pf[0], p.pf_bytes[0]);
+            prefetch_share(p.pf[1], p.pf_bytes[1]);
+#endif
         }
         return;
     }
 
     pdl_wait();
-    stage_x<QT, MAXB, XMODE>(p.x, p.ldx, static_cast<int64_t>(u0) * kUnitWeights, kseg, batch, xs, xsum, xfac, red,
+    if (tid == 0) PHB_TRACE_EV(p.trace_id, 1);
+    stage_x<CW, MAXB, XMODE>(p.x, p.ldx, static_cast<int64_t>(u0) * kUnitWeights, kseg, batch, xs, xsum, xfac, red,
                              p.gather_group, p.gather_hd, p.gather_v_off);
-    int s = 0;
-    if (!consume_tile<QT, MAXB>(t, NMAT, smem, full, empty, s, xs, xpad_len(kseg), xsum, kseg / 32, xfac, batch, part,
-                                row_acc))
-        return;
-
-    for (int it = tid; it < t.rows_here * batch; it += kConsumers) {
-        const int rr = it / batch;
-        const int b = it - rr * batch;
-        const int64_t n = row0 + rr;
-        const float a0 = row_acc[rr * kAccStride + b];
-        if (gridDim.y > 1) {
+    if (tid == 0) PHB_TRACE_EV(p.trace_id, 2);
+#ifdef PHB_EXP_XFIRST
+    if (tid == 0) mbar_arrive(xready);
+#endif
+    const bool split_out = gridDim.y > 1;
+    auto epi = [&](int r, int b, float a0, float a1) {
+        const int64_t n = row0 + r;
+        if (split_out) {
             p.part[(static_cast<int64_t>(split) * batch + b) * p.n + n] = a0;
         } else if constexpr (EPI == kEpiStore) {
             p.y[b * p.ldy + n] = a0;
         } else if constexpr (EPI == kEpiResid) {
             p.y[b * p.ldy + n] = p.r[b * p.ldr + n] + a0;
         } else {
-            const float a1 = row_acc[(t.rows_here + rr) * kAccStride + b];
             p.y[b * p.ldy + n] = silu_mul(a0, a1);
         }
+    };
+    int s = 0;
+#ifdef PHB_TRACE
+    if (tid == 0) {
+        mbar_wait(&full[0], 0, &g_dev_err);
+        PHB_TRACE_EV(p.trace_id, 3);
     }
+#endif
+    consume_tile<QT, CW, MAXB, NMAT>(t, p.sum_mode, smem, full, empty, s, xs, xpad_len(kseg), xsum, kseg / 32, xfac,
+                                     batch, part, row_acc, epi);
+    if (tid == 0) PHB_TRACE_EV(p.trace_id, 4);
 }
 
 // Host-side plan of one streaming GEMV launch.
 struct GemvPlan {
     dim3 grid;
     size_t smem;
+    int cw;                // consumer warps of the chosen instantiation
     GemvParams p;
 };
 

@@ -27,49 +27,79 @@ inline int plan_ksplit(const GemvReq& q) {
     return static_cast<int>(cdiv(units_row, seg));
 }
 
+// Eight consumer warps: a CTA takes about half an SM, so the next kernel in
+// a programmatic-dependent chain can be resident and stream its weights
+// while this one finishes.
+constexpr int cw_for(int) { return 8; }
+
 // Dynamic shared memory of a streaming-GEMV CTA:
-//   stages | xs [batch][xpad_len(kseg)] | xsum [batch][kseg/32] |
-//   part [kAccStride][256] | row_acc [nmat*rows][kAccStride] | mbarriers | red | xfac | row list
+//   stages | xs [maxb][xpad_len(kseg)] | xsum [maxb][kseg/32] |
+//   part (row-sum mode dependent) | row_acc [nmat*rows][kAccStride] (fold) |
+//   mbarriers | xfac, reduction scratch, row list
 struct SmemLayout {
     uint32_t xs, xsum, part, acc, bar;
     size_t total;
+    int sum_mode;
 };
 
-inline SmemLayout stream_smem_layout(int qt, int nmat, int xrows, int rows_per_cta, int units_seg) {
+constexpr size_t kTilePartBudget = 48 * 1024;
+
+#ifndef PHB_CTAS_PER_SM
+#define PHB_CTAS_PER_SM 2
+#endif
+// CTAs of one GEMV per SM. Two half-SM CTAs measured fastest for the chained
+// decode GEMVs (a 24-layer Q8_0 step: 550 us with 2, 775 us with 1).
+constexpr int kCtasPerSm = PHB_CTAS_PER_SM;
+
+inline SmemLayout stream_smem_layout(int qt, int cw, int nmat, int maxb, int rows_per_cta, int units_seg) {
     const int ub = qt == 0 ? Fmt<0>::unit_bytes : Fmt<1>::unit_bytes;
-    const int ns = qt == 0 ? StageCfg<0>::ns : StageCfg<1>::ns;
+    const int consumers = 32 * cw;
+    const int stage_units = consumers / 2;
+    const int ns = qt == 0 ? 2 : 3;
     SmemLayout l{};
-    size_t off = static_cast<size_t>(ns) * kStageUnits * ub;
+    size_t off = static_cast<size_t>(ns) * stage_units * ub;
     const size_t kseg = static_cast<size_t>(units_seg) * kUnitWeights;
     l.xs = static_cast<uint32_t>(off);
-    off += static_cast<size_t>(xrows) * xpad_len(static_cast<int>(kseg)) * sizeof(float);
+    off += static_cast<size_t>(maxb) * xpad_len(static_cast<int>(kseg)) * sizeof(float);
     l.xsum = static_cast<uint32_t>(off);
-    off += static_cast<size_t>(xrows) * (kseg / 32) * sizeof(float);
+    off += static_cast<size_t>(maxb) * (kseg / 32) * sizeof(float);
     l.part = static_cast<uint32_t>(off);
-    off += static_cast<size_t>(2 * kStageUnits) * kAccStride * sizeof(float);
+    const size_t tile_part = 2 * static_cast<size_t>(nmat) * rows_per_cta * units_seg * maxb * sizeof(float);
+    if (warp_rows(units_seg, nmat)) {
+        l.sum_mode = kSumWarp;
+    } else if (tile_part <= kTilePartBudget) {
+        l.sum_mode = kSumTile;
+        off += tile_part;
+    } else {
+        l.sum_mode = kSumFold;
+        off += static_cast<size_t>(maxb) * consumers * sizeof(float);
+    }
     l.acc = static_cast<uint32_t>(off);
-    off += static_cast<size_t>(nmat) * rows_per_cta * kAccStride * sizeof(float);
+    if (l.sum_mode == kSumFold) off += static_cast<size_t>(nmat) * rows_per_cta * kAccStride * sizeof(float);
+    off = (off + 15) & ~static_cast<size_t>(15);
     l.bar = static_cast<uint32_t>(off);
     off += 2 * ns * sizeof(uint64_t);
-    off += static_cast<size_t>(kConsumerWarps + 3) * kAccStride * sizeof(float);  // red, xfac, row list
+    off += kTailFloats * sizeof(float);  // xfac, reduction scratch, row list
     l.total = off;
     return l;
 }
 
-// Fill a launch plan. Returns false if no layout fits shared memory.
+// Fill a launch plan (one CTA per SM per K split). Returns false if no
+// layout fits shared memory.
 inline bool plan_stream(const GemvReq& q, GemvPlan* pl) {
     const int units_row = static_cast<int>(q.k / kUnitWeights);
     const int ksplit0 = plan_ksplit(q);
     const int units_seg = static_cast<int>(cdiv(units_row, ksplit0));
     const int ksplit = static_cast<int>(cdiv(units_row, units_seg));
     const int maxb = maxb_for(q.batch);
+    const int cw = cw_for(maxb);
     const int sms = device_sm_count();
-    const int64_t target = std::max<int64_t>(1, cdiv(2 * static_cast<int64_t>(sms), ksplit));
+    const int64_t target = std::max<int64_t>(1, cdiv(static_cast<int64_t>(sms) * kCtasPerSm, ksplit));
     int64_t nrow_ctas = std::min<int64_t>(q.n, target);
     int rows_per_cta = static_cast<int>(cdiv(q.n, nrow_ctas));
     SmemLayout lay{};
     for (;;) {
-        lay = stream_smem_layout(q.qt, q.nmat, q.batch, rows_per_cta, units_seg);
+        lay = stream_smem_layout(q.qt, cw, q.nmat, maxb, rows_per_cta, units_seg);
         if (lay.total <= kSmemOptin) break;
         if (rows_per_cta == 1) return false;
         rows_per_cta = (rows_per_cta + 1) / 2;
@@ -85,6 +115,7 @@ inline bool plan_stream(const GemvReq& q, GemvPlan* pl) {
     p.units_seg = units_seg;
     p.rows_per_cta = rows_per_cta;
     p.batch = q.batch;
+    p.sum_mode = lay.sum_mode;
     p.x = q.x;
     p.ldx = q.ldx;
     p.y = q.y;
@@ -95,22 +126,29 @@ inline bool plan_stream(const GemvReq& q, GemvPlan* pl) {
     p.gather_group = q.gather_group;
     p.gather_hd = q.gather_hd;
     p.gather_v_off = q.gather_v_off;
+    for (int i = 0; i < 2; ++i) {
+        p.pf[i] = static_cast<const uint8_t*>(q.pf[i]);
+        p.pf_bytes[i] = q.pf_bytes[i];
+    }
     p.xs_off = lay.xs;
     p.xsum_off = lay.xsum;
     p.part_off = lay.part;
     p.acc_off = lay.acc;
     p.bar_off = lay.bar;
+    p.trace_id = q.trace_id;
     pl->grid = dim3(static_cast<unsigned>(nrow_ctas), static_cast<unsigned>(ksplit), 1);
     pl->smem = lay.total;
+    pl->cw = cw;
     return true;
 }
 
 template <int QT, int MAXB, int NMAT, int XMODE, int EPI>
 inline cudaError_t run_stream(const GemvPlan& pl, cudaStream_t s, bool pdl) {
-    constexpr auto kern = gemv_stream_kernel<QT, MAXB, NMAT, XMODE, EPI>;
+    constexpr int CW = cw_for(MAXB);
+    constexpr auto kern = gemv_stream_kernel<QT, CW, MAXB, NMAT, XMODE, EPI>;
     cudaError_t e = ensure_smem_attr<kern>();
     if (e != cudaSuccess) return e;
-    return launch_kernel(kern, pl.grid, dim3(kGemvThreads), pl.smem, s, pdl, pl.p);
+    return launch_kernel(kern, pl.grid, dim3(KCfg<QT, CW>::threads), pl.smem, s, pdl, pl.p);
 }
 
 }  // namespace phb

@@ -38,6 +38,7 @@ constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 8;
 constexpr int kMaxTokens = 64;
 constexpr int kMoeGroup = 8;  // tokens per pass over a staged weight tile
+constexpr int kMoeCW = 8;     // consumer warps of the grouped kernels
 
 struct RouteOut {
     int32_t* idx;        // [T][k]
@@ -155,6 +156,9 @@ struct MoeParams {
     float* y;                 // [pairs][n]
     int64_t ldy;
     RouteOut r;
+    int sum_mode;
+    const uint8_t* pf;        // per-expert matrix to prefetch into L2 (the down matrix), or null
+    int64_t pf_stride;        // its bytes per expert
     uint32_t xs_off, xsum_off, part_off, acc_off, bar_off;
 };
 
@@ -165,41 +169,37 @@ __device__ __forceinline__ bool moe_group(const MoeParams& p, const Tile& t, int
     float* xsum = reinterpret_cast<float*>(smem + p.xsum_off);
     float* part = reinterpret_cast<float*>(smem + p.part_off);
     float* row_acc = reinterpret_cast<float*>(smem + p.acc_off);
-    float* red = reinterpret_cast<float*>(smem + p.bar_off + 2 * StageCfg<QT>::ns * sizeof(uint64_t));
-    float* xfac = red + (kConsumerWarps + 1) * kAccStride;
-    int* rowidx = reinterpret_cast<int*>(xfac + kAccStride);
+    float* xfac = reinterpret_cast<float*>(full + 2 * KCfg<QT, kMoeCW>::ns);
+    float* red = xfac + kAccStride;
+    int* rowidx = reinterpret_cast<int*>(red + (2 * kMaxConsumerWarps + 3) * kAccStride);
     const int tid = threadIdx.x;
     const int kseg = t.useg * kUnitWeights;
     if (tid < nb) {
         const int pair = p.r.pair_list[first_pair_idx + tid];
         rowidx[tid] = p.x_by_pair ? pair : pair / p.top_k;
     }
-    for (int i = tid; i < NMAT * t.rows_here * kAccStride; i += kConsumers) row_acc[i] = 0.f;
-    consumer_sync();
-    stage_x<QT, MAXB, kXRowList>(p.x, p.ldx, 0, kseg, nb, xs, xsum, xfac, red, 1, 1, 0, rowidx);
-    if (!consume_tile<QT, MAXB>(t, NMAT, smem, full, empty, s, xs, xpad_len(kseg), xsum, kseg / 32, xfac, nb, part,
-                                row_acc))
+    if (p.sum_mode == kSumFold)
+        for (int i = tid; i < NMAT * t.rows_here * kAccStride; i += KCfg<QT, kMoeCW>::consumers) row_acc[i] = 0.f;
+    consumer_sync<KCfg<QT, kMoeCW>::consumers>();
+    stage_x<kMoeCW, MAXB, kXRowList>(p.x, p.ldx, 0, kseg, nb, xs, xsum, xfac, red, 1, 1, 0, rowidx);
+    const int* pairs = p.r.pair_list + first_pair_idx;
+    auto epi = [&](int r, int b, float a0, float a1) {
+        const float out = NMAT == 2 ? silu_mul(a0, a1) : a0;
+        p.y[static_cast<int64_t>(pairs[b]) * p.ldy + row0 + r] = out;
+    };
+    if (!consume_tile<QT, kMoeCW, MAXB, NMAT>(t, p.sum_mode, smem, full, empty, s, xs, xpad_len(kseg), xsum,
+                                              kseg / 32, xfac, nb, part, row_acc, epi))
         return false;
-    for (int it = tid; it < t.rows_here * nb; it += kConsumers) {
-        const int rr = it / nb;
-        const int b = it - rr * nb;
-        const int pair = p.r.pair_list[first_pair_idx + b];
-        const float a0 = row_acc[rr * kAccStride + b];
-        float out = a0;
-        if constexpr (NMAT == 2) out = silu_mul(a0, row_acc[(t.rows_here + rr) * kAccStride + b]);
-        p.y[static_cast<int64_t>(pair) * p.ldy + row0 + rr] = out;
-    }
-    consumer_sync();
+    consumer_sync<KCfg<QT, kMoeCW>::consumers>();  // the next group overwrites xs, xsum and row_acc
     return true;
 }
 
 template <int QT, int NMAT>
-__global__ void __launch_bounds__(kGemvThreads, 1) moe_stream_kernel(const __grid_constant__ MoeParams p) {
+__global__ void __launch_bounds__(KCfg<QT, kMoeCW>::threads, 1) moe_stream_kernel(const __grid_constant__ MoeParams p) {
+    using C = KCfg<QT, kMoeCW>;
     extern __shared__ __align__(1024) uint8_t smem[];
-    constexpr int NS = StageCfg<QT>::ns;
-    constexpr int UB = Fmt<QT>::unit_bytes;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
-    uint64_t* empty = full + NS;
+    uint64_t* empty = full + C::ns;
     pdl_launch_dependents();
     pdl_wait();  // routing results (and, for the down pass, h) come from the previous kernels
     const int slot = blockIdx.y;
@@ -216,23 +216,27 @@ __global__ void __launch_bounds__(kGemvThreads, 1) moe_stream_kernel(const __gri
     t.contiguous = true;
     t.w[0] = p.w[0] + e * p.expert_stride + static_cast<int64_t>(row0) * p.row_bytes;
     t.w[1] = p.w[NMAT - 1] + e * p.expert_stride + static_cast<int64_t>(row0) * p.row_bytes;
-    (void)UB;
     const int tid = threadIdx.x;
     if (tid == 0) {
-        for (int s = 0; s < NS; ++s) {
+        for (int s = 0; s < C::ns; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumerWarps);
+            mbar_init(&empty[s], kMoeCW);
         }
         fence_barrier_init();
     }
     __syncthreads();
     const int ngroups = (cnt + kMoeGroup - 1) / kMoeGroup;
-    if (tid >= kConsumers) {
-        if (tid == kConsumers) {
+    if (tid >= C::consumers) {
+        if (tid == C::consumers) {
             const uint64_t pol = policy_evict_first();
             int s = 0;
             for (int gi = 0; gi < ngroups; ++gi)
-                if (!produce_tile<QT>(t, NMAT, smem, full, empty, s, pol)) break;
+                if (!produce_tile<QT, kMoeCW>(t, NMAT, smem, full, empty, s, pol)) break;
+        } else if (tid == C::consumers + 1 && p.pf != nullptr && blockIdx.x == 0) {
+            // the expert's down matrix, needed by the next kernel
+            const uint8_t* base = p.pf + e * p.pf_stride;
+            for (int64_t off = 0; off < p.pf_stride; off += 32768)
+                prefetch_l2(base + off, static_cast<uint32_t>(p.pf_stride - off < 32768 ? p.pf_stride - off : 32768));
         }
         return;
     }
@@ -303,7 +307,7 @@ cudaError_t launch_moe_stream(const MoeParams& p, dim3 grid, size_t smem, cudaSt
     constexpr auto kern = moe_stream_kernel<QT, NMAT>;
     cudaError_t e = ensure_smem_attr<kern>();
     if (e != cudaSuccess) return e;
-    return launch_kernel(kern, grid, dim3(kGemvThreads), smem, s, true, p);
+    return launch_kernel(kern, grid, dim3(KCfg<QT, kMoeCW>::threads), smem, s, true, p);
 }
 
 // Rows per CTA and shared-memory layout of one grouped pass.
@@ -312,7 +316,7 @@ bool plan_moe(int qt, int nmat, int64_t n, int64_t k, int cpe, MoeParams* p, uns
     int rows_per_cta = static_cast<int>(cdiv(n, cpe));
     SmemLayout lay{};
     for (;;) {
-        lay = stream_smem_layout(qt, nmat, kMoeGroup, rows_per_cta, units_row);
+        lay = stream_smem_layout(qt, kMoeCW, nmat, kMoeGroup, rows_per_cta, units_row);
         if (lay.total <= kSmemOptin) break;
         if (rows_per_cta == 1) return false;
         rows_per_cta = (rows_per_cta + 1) / 2;
@@ -322,6 +326,7 @@ bool plan_moe(int qt, int nmat, int64_t n, int64_t k, int cpe, MoeParams* p, uns
     p->row_bytes = static_cast<int64_t>(units_row) * (qt == 0 ? Fmt<0>::unit_bytes : Fmt<1>::unit_bytes);
     p->n = n;
     p->expert_stride = n * p->row_bytes;
+    p->sum_mode = lay.sum_mode;
     p->xs_off = lay.xs;
     p->xsum_off = lay.xsum;
     p->part_off = lay.part;
@@ -362,6 +367,8 @@ cudaError_t moe_run(const MoeReq& q, cudaStream_t s) {
     pg.y = w.h;
     pg.ldy = q.d_ff;
     pg.r = w.r;
+    pg.pf = static_cast<const uint8_t*>(q.wd);
+    pg.pf_stride = q.d_model * static_cast<int64_t>(q.qt == 0 ? q.d_ff / 32 * 34 : q.d_ff / 256 * 144);
     e = q.qt == 0 ? launch_moe_stream<0, 2>(pg, dim3(gx, slots), smem, s)
                   : launch_moe_stream<1, 2>(pg, dim3(gx, slots), smem, s);
     if (e != cudaSuccess) return e;

@@ -26,8 +26,8 @@ template <> struct Fmt<1> { static constexpr int unit_bytes = 144; };  // Q4_K
 // Device error codes written to a kernel's error word.
 constexpr int kDevErrTimeout = 1;
 
-// Upper bound on mbarrier polls before a wait is declared stuck. Each
-// try_wait may suspend the thread for a while, so this is seconds of wall time.
+// Upper bound on mbarrier polls before a wait is declared stuck (the wall
+// clock bound kWaitLimitNs below normally ends a stuck wait first).
 constexpr uint32_t kSpinLimit = 1u << 26;
 
 __device__ __forceinline__ float fp16_bits_to_float(uint32_t bits16) {
@@ -72,26 +72,53 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
+// One poll of phase `parity`; a thread whose phase is not yet complete may
+// be suspended for up to about kSuspendHintNs before the call returns false.
+constexpr uint32_t kSuspendHintNs = 20000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity)
+        : "r"(smem_addr(bar)), "r"(parity), "n"(kSuspendHintNs)
         : "memory");
     return ok != 0;
 }
 
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wall-clock bound of any single wait.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
 // Bounded wait on phase `parity` of `bar`. Returns false (and records the
-// timeout in *err) when the phase did not complete within kSpinLimit polls.
+// timeout in *err) when the phase did not complete within kWaitLimitNs.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
     for (uint32_t i = 0; i < kSpinLimit; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > kWaitLimitNs) break;
     }
     atomicExch(err, kDevErrTimeout);
     return false;
+}
+
+// Warp-wide bounded wait: lane 0 polls, the other lanes wait at the warp
+// barrier, then every lane acquires the completed phase itself (one poll).
+// All 32 lanes must call it.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int* err) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, err) ? 1 : 0;
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    if (!ok) return false;
+    return mbar_wait(bar, parity, err);
 }
 
 // ---------------------------------------------------------------- PTX: bulk copies

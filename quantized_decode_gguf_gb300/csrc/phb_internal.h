@@ -23,6 +23,12 @@ inline cudaError_t ensure_smem_attr() {
     if (mask.load(std::memory_order_acquire) & bit) return cudaSuccess;
     e = cudaFuncSetAttribute(reinterpret_cast<const void*>(KERN), cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmemOptin));
+    // Every kernel asks for the largest shared-memory carveout, so kernels of
+    // a programmatic-dependent chain share one SM configuration and the next
+    // kernel's CTAs can be resident beside the current one's.
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(reinterpret_cast<const void*>(KERN), cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 static_cast<int>(cudaSharedmemCarveoutMaxShared));
     if (e == cudaSuccess) mask.fetch_or(bit, std::memory_order_acq_rel);
     return e;
 }
@@ -68,6 +74,9 @@ struct GemvReq {
     float* ws = nullptr;          // split-K partials
     size_t ws_floats = 0;
     bool pdl = true;
+    const void* pf[2] = {nullptr, nullptr};  // weights of later kernels to prefetch into L2
+    int64_t pf_bytes[2] = {0, 0};
+    int trace_id = -1;            // launch id recorded by debug tracing builds
 };
 
 // Workspace floats gemv_run needs for this request (split-K partials).
