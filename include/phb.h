@@ -202,6 +202,27 @@ phb_status phb_decode_step(int qtype, const phb_dense_layer* layers, int n_layer
                            const float* x_in, float* x_out,
                            void* ws, size_t ws_bytes, phb_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * SwiGLU feed-forward block that allocates nothing. The paper has no
+ * counterpart; this is a convenience for callers that cannot allocate
+ * device memory (a serving loop whose memory budget is fixed at start-up,
+ * or a plugin running inside another runtime that owns all device memory).
+ * Same arguments, result and bounds as phb_ffn_swiglu, minus the workspace:
+ * the scratch is a static device array of
+ * phb_ffn_swiglu_noalloc_max_scratch() bytes (2 MiB) compiled into the
+ * library, which every GPU that loads the library holds until the process
+ * exits. A shape whose phb_ffn_swiglu_workspace_size exceeds it returns
+ * PHB_ERR_WORKSPACE. The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress); make that first call before any
+ * stream capture. Every call on a device uses the same array, which keeps
+ * the previous call's contents (nothing in it needs to start at zero):
+ * calls whose GPU work overlaps (other streams, other host threads) race.
+ * ------------------------------------------------------------------------- */
+size_t phb_ffn_swiglu_noalloc_max_scratch(void);
+phb_status phb_ffn_swiglu_noalloc(int qtype, const void* Wgate, const void* Wup, const void* Wdown,
+                                  const float* X, float* Y, int64_t d_model, int64_t d_ff, int batch,
+                                  phb_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

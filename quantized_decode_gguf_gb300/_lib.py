@@ -39,6 +39,8 @@ SIGNATURES = {
                              _c_int, _c_vp, _c_vp, _c_vp, _c_sz, _c_vp]),
     "phb_gemm_q_prefill_workspace_size": (_c_sz, [_c_int, _c_i64, _c_i64, _c_i64]),
     "phb_gemm_q_prefill": (_c_int, [_c_int, _c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64, _c_vp, _c_sz, _c_vp]),
+    "phb_ffn_swiglu_noalloc_max_scratch": (_c_sz, []),
+    "phb_ffn_swiglu_noalloc": (_c_int, [_c_int, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_int, _c_vp]),
     "phb_decode_step_workspace_size": (_c_sz, [_c_int, _c_i64, _c_int, _c_int, _c_int, _c_i64]),
     "phb_decode_step": (_c_int, [_c_int, _c_vp, _c_int, _c_i64, _c_int, _c_int, _c_int, _c_i64, _c_vp, _c_vp, _c_vp,
                                  _c_sz, _c_vp]),

@@ -178,6 +178,18 @@ DecodeWs decode_ws(int64_t d_model, int n_q, int n_kv, int hd, int64_t d_ff, voi
 
 }  // namespace
 
+namespace phb {
+phb_status set_last_error(phb_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+}  // namespace phb
+
 extern "C" {
 
 int phb_version(void) { return 10000; }

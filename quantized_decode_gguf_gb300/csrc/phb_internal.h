@@ -6,7 +6,12 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "phb.h"
+
 namespace phb {
+
+// Record the message of a failed call for phb_last_error() and return `s`.
+phb_status set_last_error(phb_status s, const char* fmt, ...);
 
 // ---------------------------------------------------------------- device info
 int device_sm_count();         // multiprocessors of the current device (cached)
