@@ -1,4 +1,31 @@
-// Prompt-processing GEMM (tcgen05). Placeholder until the tensor-core kernel lands.
+// Prompt-processing GEMM on the 5th-generation tensor cores (tcgen05).
+//
+//   Y[t][n] = sum_k bf16(w[n][k]) * bf16(X[t][k]),  fp32 accumulation.
+//
+// The weights are the MMA's M operand: a CTA owns 128 weight rows and 256
+// tokens (D = 128 x 256 fp32 in TMEM, 256 columns). Per 64-wide K block:
+//  - four producer warps dequantise their rows (one row per thread, raw
+//    blocks double-buffered in registers from global memory) to bf16 and
+//    store them in the 128-byte-swizzled K-major layout the MMA reads;
+//  - one thread loads the token tile (bf16, 256 x 64) with a 2-D TMA copy
+//    into the same swizzled layout;
+//  - one thread issues four tcgen05.mma (M128 N256 K16) and commits them to
+//    the stage's "empty" barrier;
+// after the last K block the four producer warps drain TMEM (tcgen05.ld,
+// one TMEM lane per weight row) and write Y, or a split-K partial that a
+// second kernel reduces in split order. X is cast to bf16 (round to nearest
+// even) by a first kernel into the caller's workspace.
+//
+// Every wait is bounded; a wait that runs out sets this translation unit's
+// device error word, the kernel drains and frees its TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "gemv_core.cuh"
+#include "phb_common.cuh"
 #include "phb_internal.h"
 
 namespace phb {
@@ -8,12 +35,464 @@ static __device__ int g_dev_err_prefill;
 cudaError_t read_dev_err_prefill(int* code) {
     int v = 0;
     cudaError_t e = cudaMemcpyFromSymbol(&v, g_dev_err_prefill, sizeof(int));
+    if (e != cudaSuccess) return e;
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_dev_err_prefill, &zero, sizeof(int));
     *code = v;
     return e;
 }
 
-size_t prefill_ws_bytes(const PrefillReq& q) { return static_cast<size_t>(q.m) * q.k * 2 + 256; }
+namespace {
 
-cudaError_t prefill_run(const PrefillReq&, cudaStream_t) { return cudaErrorNotSupported; }
+constexpr int kBM = 128;                   // weight rows per CTA (MMA M)
+constexpr int kBN = 256;                   // tokens per CTA (MMA N)
+constexpr int kBK = 64;                    // K per stage: one 128-byte bf16 row
+constexpr int kStages = 4;
+constexpr int kATile = kBM * kBK * 2;      // 16 KB
+constexpr int kBTile = kBN * kBK * 2;      // 32 KB
+constexpr int kThreads = 256;
+constexpr int kProducerWarps = 4;          // warps 0-3: dequant producers, then epilogue
+constexpr int kTmaWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr uint32_t kTmemCols = 256;
+constexpr int kKbPerUnit = 4;              // a 256-weight unit spans four K blocks
+constexpr size_t kSmemBytes = kStages * (kATile + kBTile) + 1024 /* align */ + 256 /* barriers */;
+
+struct PrefillParams {
+    const uint8_t* w;
+    int64_t row_bytes;
+    int64_t n, m, k;
+    int units_per_split;  // 256-weight units of K per split
+    int n_units;          // K / 256
+    float* y;             // [m][n]
+    float* part;          // [splits][m][n] when gridDim.z > 1
+};
+
+// ---------------------------------------------------------------- tcgen05 / TMA PTX
+__device__ __forceinline__ uint64_t smem_desc_sw128(const void* p) {
+    // K-major operand in the 128-byte swizzle layout: 8-row groups of
+    // 128-byte rows, 1024 bytes apart (stride byte offset); version 1.
+    const uint64_t addr = smem_addr(p);
+    return ((addr & 0x3FFFFull) >> 4) | (1ull << 16) | ((1024ull >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// kind::f16, D fp32, A and B bf16, both K-major, M = 128, N = 256.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(kBN >> 3) << 17) | (uint32_t(kBM >> 4) << 24);
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// 32 consecutive TMEM columns of this warp's 32 lanes, one lane per thread.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ---------------------------------------------------------------- dequant to swizzled bf16
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    const __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&t);
+}
+
+// Store 16-byte chunk `ch` (8 bf16, k = 8ch..8ch+7) of tile row `row`.
+__device__ __forceinline__ void st_chunk(uint8_t* tile, int row, int ch, uint32_t a, uint32_t b, uint32_t c,
+                                         uint32_t d) {
+    uint4* dst = reinterpret_cast<uint4*>(tile + row * 128 + ((ch ^ (row & 7)) << 4));
+    *dst = make_uint4(a, b, c, d);
+}
+
+// Exact small-integer conversion: 0x4B0000bb is the float 2^23 + bb.
+template <int SEL>
+__device__ __forceinline__ float byte_int(uint32_t w, float bias) {
+    return __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7440u | SEL)) - bias;
+}
+
+// One K block (64 weights) of a Q8_0 unit held in registers (68 words).
+template <int J>
+__device__ __forceinline__ void dequant_q8_0_kb(const uint32_t (&u)[68], uint8_t* tile, int row) {
+#pragma unroll
+    for (int hb = 0; hb < 2; ++hb) {
+        const int ob = 68 * J + 34 * hb;  // byte offset of the block in the unit
+        const uint32_t dw = u[ob / 4];
+        const float d = fp16_bits_to_float((ob % 4) ? (dw >> 16) : dw);
+        float w[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int p = ob + 2 + i;
+            const uint32_t word = u[p / 4] ^ 0x80808080u;
+            float q;
+            switch (p % 4) {
+                case 0: q = byte_int<0>(word, 8388736.0f); break;
+                case 1: q = byte_int<1>(word, 8388736.0f); break;
+                case 2: q = byte_int<2>(word, 8388736.0f); break;
+                default: q = byte_int<3>(word, 8388736.0f); break;
+            }
+            w[i] = d * q;  // exact
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            st_chunk(tile, row, 4 * hb + c, pack_bf16(w[8 * c], w[8 * c + 1]), pack_bf16(w[8 * c + 2], w[8 * c + 3]),
+                     pack_bf16(w[8 * c + 4], w[8 * c + 5]), pack_bf16(w[8 * c + 6], w[8 * c + 7]));
+    }
+}
+
+// One K block (64 weights: sub-blocks 2J and 2J+1) of a Q4_K block in registers (36 words).
+template <int J>
+__device__ __forceinline__ void dequant_q4_k_kb(const uint32_t (&u)[36], uint8_t* tile, int row) {
+    const float d = fp16_bits_to_float(u[0]);
+    const float dmin = fp16_bits_to_float(u[0] >> 16);
+    const uint32_t sw[3] = {u[1], u[2], u[3]};
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        uint32_t sc, m;
+        q4_k_scale_min(sw, 2 * J + half, sc, m);
+        const float D = d * static_cast<float>(sc);     // exact
+        const float M = dmin * static_cast<float>(m);   // exact
+        float w[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const uint32_t word = u[4 + 8 * J + i / 4];
+            const uint32_t nib = (half ? (word >> 4) : word) & 0x0F0F0F0Fu;
+            float q;
+            switch (i % 4) {
+                case 0: q = byte_int<0>(nib, 8388608.0f); break;
+                case 1: q = byte_int<1>(nib, 8388608.0f); break;
+                case 2: q = byte_int<2>(nib, 8388608.0f); break;
+                default: q = byte_int<3>(nib, 8388608.0f); break;
+            }
+            w[i] = fmaf(D, q, -M);  // one rounding of the exact D*q - M
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            st_chunk(tile, row, 4 * half + c, pack_bf16(w[8 * c], w[8 * c + 1]), pack_bf16(w[8 * c + 2], w[8 * c + 3]),
+                     pack_bf16(w[8 * c + 4], w[8 * c + 5]), pack_bf16(w[8 * c + 6], w[8 * c + 7]));
+    }
+}
+
+template <int NW>
+__device__ __forceinline__ void load_unit(const uint8_t* src, uint32_t (&u)[NW]) {
+#pragma unroll
+    for (int i = 0; i < NW / 4; ++i) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(src) + i);
+        u[4 * i] = v.x;
+        u[4 * i + 1] = v.y;
+        u[4 * i + 2] = v.z;
+        u[4 * i + 3] = v.w;
+    }
+}
+
+// ---------------------------------------------------------------- the GEMM kernel
+template <int QT>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ PrefillParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t{1023});
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + kStages * kATile;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStages * kBTile);
+    uint64_t* empty = full + kStages;
+    uint64_t* accb = empty + kStages;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kBM;
+    const int t0 = blockIdx.y * kBN;
+    const int split = blockIdx.z;
+    const int u0 = split * p.units_per_split;
+    const int nu = min(p.units_per_split, p.n_units - u0);
+    const int nkb = nu * kKbPerUnit;
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], kProducerWarps + 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(accb, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == kMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    pdl_launch_dependents();
+
+    if (warp < kProducerWarps) {
+        // ---------------- dequant producers: thread tid owns weight row n0 + tid
+        const int row = tid;
+        const uint8_t* wr = p.w + (n0 + row) * p.row_bytes;
+        constexpr int UB = QT == 0 ? 272 : 144;
+        constexpr int NW = UB / 4;
+        uint32_t cur[NW], nxt[NW];
+        if (nu > 0) load_unit<NW>(wr + static_cast<int64_t>(u0) * UB, cur);
+        for (int uu = 0; uu < nu; ++uu) {
+            if (uu + 1 < nu) load_unit<NW>(wr + static_cast<int64_t>(u0 + uu + 1) * UB, nxt);
+#pragma unroll
+            for (int j = 0; j < kKbPerUnit; ++j) {
+                const int i = uu * kKbPerUnit + j;
+                const int s = i % kStages;
+                if (i >= kStages && !mbar_wait_warp(&empty[s], ((i / kStages) - 1) & 1, &g_dev_err_prefill)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                uint8_t* tile = sA + s * kATile;
+                if constexpr (QT == 0) {
+                    if (j == 0) dequant_q8_0_kb<0>(cur, tile, row);
+                    else if (j == 1) dequant_q8_0_kb<1>(cur, tile, row);
+                    else if (j == 2) dequant_q8_0_kb<2>(cur, tile, row);
+                    else dequant_q8_0_kb<3>(cur, tile, row);
+                } else {
+                    if (j == 0) dequant_q4_k_kb<0>(cur, tile, row);
+                    else if (j == 1) dequant_q4_k_kb<1>(cur, tile, row);
+                    else if (j == 2) dequant_q4_k_kb<2>(cur, tile, row);
+                    else dequant_q4_k_kb<3>(cur, tile, row);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full[s]);
+            }
+            if (*abort_flag) break;
+#pragma unroll
+            for (int i = 0; i < NW; ++i) cur[i] = nxt[i];
+        }
+    } else if (warp == kTmaWarp) {
+        // ---------------- token tiles by TMA
+        if (lane == 0) {
+            pdl_wait();  // the bf16 copy of X comes from the previous kernel
+            for (int i = 0; i < nkb; ++i) {
+                const int s = i % kStages;
+                if (i >= kStages && !mbar_wait(&empty[s], ((i / kStages) - 1) & 1, &g_dev_err_prefill)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                mbar_arrive_expect_tx(&full[s], kBTile);
+                tma_load_2d(sB + s * kBTile, &tmap_x, (u0 * kKbPerUnit + i) * kBK, t0, &full[s]);
+            }
+            // Before the CTA can exit, every copy issued into shared memory must
+            // have landed: wait (bounded) on the last phase of each slot. On the
+            // normal path these phases completed long ago.
+            for (int i = max(0, nkb - kStages); i < nkb; ++i)
+                mbar_wait(&full[i % kStages], (i / kStages) & 1, &g_dev_err_prefill);
+        }
+    } else if (warp == kMmaWarp) {
+        // ---------------- one thread issues the MMAs
+        if (lane == 0) {
+            bool ok = true;
+            for (int i = 0; i < nkb; ++i) {
+                const int s = i % kStages;
+                if (!mbar_wait(&full[s], (i / kStages) & 1, &g_dev_err_prefill)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk) {
+                    const uint64_t ad = smem_desc_sw128(sA + s * kATile + kk * 32);
+                    const uint64_t bd = smem_desc_sw128(sB + s * kBTile + kk * 32);
+                    mma_bf16(tmem, ad, bd, (i > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(&empty[s]);
+            }
+            if (!ok) *abort_flag = 1;
+            mma_commit(accb);  // arrives once every MMA issued above has completed
+        }
+    }
+
+    // ---------------- epilogue: warps 0-3 drain TMEM lanes 0..127 (one weight row each)
+    if (warp < kProducerWarps) {
+        pdl_wait();  // outputs may still be read by the previous kernel
+        const bool ready = mbar_wait_warp(accb, 0, &g_dev_err_prefill);
+        tc_fence_after();
+        if (ready && !*abort_flag && nkb > 0) {
+            const int64_t n = n0 + 32 * warp + lane;
+            float* out = gridDim.z > 1 ? p.part + static_cast<int64_t>(split) * p.m * p.n : p.y;
+#pragma unroll 1
+            for (int c0 = 0; c0 < kBN; c0 += 32) {
+                float v[32];
+                tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + c0, v);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int t = t0 + c0 + j;
+                    if (t < p.m) out[static_cast<int64_t>(t) * p.n + n] = v[j];
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        // every MMA issued has completed once accb has arrived (bounded wait)
+        mbar_wait_warp(accb, 0, &g_dev_err_prefill);
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    }
+}
+
+// X fp32 [m][k] -> bf16 (round to nearest even), 8 values per thread.
+__global__ void __launch_bounds__(256) cast_bf16_kernel(const float* __restrict__ x, uint32_t* __restrict__ xb,
+                                                        int64_t count8) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < count8; i += stride) {
+        const float4 a = reinterpret_cast<const float4*>(x)[2 * i];
+        const float4 b = reinterpret_cast<const float4*>(x)[2 * i + 1];
+        reinterpret_cast<uint4*>(xb)[i] =
+            make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(b.x, b.y), pack_bf16(b.z, b.w));
+    }
+}
+
+// Y = sum over splits in split order.
+__global__ void __launch_bounds__(256) prefill_reduce_kernel(const float4* __restrict__ part, float4* __restrict__ y,
+                                                             int64_t count4, int splits) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < count4; i += stride) {
+        float4 acc = part[i];
+        for (int s = 1; s < splits; ++s) {
+            const float4 v = part[static_cast<int64_t>(s) * count4 + i];
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        y[i] = acc;
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+struct SplitPlan {
+    int splits;
+    int units_per_split;
+};
+
+SplitPlan plan_splits(int64_t m, int64_t n, int64_t k) {
+    const int n_units = static_cast<int>(k / kUnitWeights);
+    const int64_t tiles = (n / kBM) * ((m + kBN - 1) / kBN);
+    const int sms = device_sm_count();
+    int splits = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(sms / std::max<int64_t>(1, tiles), n_units)));
+    const int ups = (n_units + splits - 1) / splits;
+    splits = (n_units + ups - 1) / ups;
+    return {splits, ups};
+}
+
+inline size_t align_up(size_t v) { return (v + 255) & ~size_t{255}; }
+
+}  // namespace
+
+size_t prefill_ws_bytes(const PrefillReq& q) {
+    const SplitPlan sp = plan_splits(q.m, q.n, q.k);
+    size_t b = align_up(static_cast<size_t>(q.m) * q.k * 2);
+    if (sp.splits > 1) b += static_cast<size_t>(sp.splits) * q.m * q.n * sizeof(float);
+    return b;
+}
+
+cudaError_t prefill_run(const PrefillReq& q, cudaStream_t s) {
+    PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode_fn();
+    if (encode == nullptr) return cudaErrorNotSupported;
+    const SplitPlan sp = plan_splits(q.m, q.n, q.k);
+    auto* ws = static_cast<uint8_t*>(q.ws);
+    uint32_t* xb = reinterpret_cast<uint32_t*>(ws);
+    float* part = reinterpret_cast<float*>(ws + align_up(static_cast<size_t>(q.m) * q.k * 2));
+
+    // token matrix (bf16 [m][k]) as a 2-D tensor: 64 x 256 boxes, 128-byte swizzle
+    CUtensorMap tmap;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(q.k), static_cast<cuuint64_t>(q.m)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(q.k) * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(kBN)};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, xb, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+
+    const int64_t count8 = q.m * q.k / 8;
+    cudaError_t e = launch_kernel(cast_bf16_kernel, dim3(static_cast<unsigned>(std::min<int64_t>(
+                                                          (count8 + 255) / 256, int64_t{device_sm_count()} * 8))),
+                                  dim3(256), 0, s, true, q.x, xb, count8);
+    if (e != cudaSuccess) return e;
+
+    PrefillParams p{};
+    p.w = static_cast<const uint8_t*>(q.w);
+    p.row_bytes = q.qt == 0 ? q.k / 32 * 34 : q.k / 256 * 144;
+    p.n = q.n;
+    p.m = q.m;
+    p.k = q.k;
+    p.units_per_split = sp.units_per_split;
+    p.n_units = static_cast<int>(q.k / kUnitWeights);
+    p.y = q.y;
+    p.part = part;
+    const dim3 grid(static_cast<unsigned>(q.n / kBM), static_cast<unsigned>((q.m + kBN - 1) / kBN),
+                    static_cast<unsigned>(sp.splits));
+    if (q.qt == 0) {
+        constexpr auto kern = prefill_gemm_kernel<0>;
+        if ((e = ensure_smem_attr<kern>()) != cudaSuccess) return e;
+        e = launch_kernel(kern, grid, dim3(kThreads), kSmemBytes, s, true, tmap, p);
+    } else {
+        constexpr auto kern = prefill_gemm_kernel<1>;
+        if ((e = ensure_smem_attr<kern>()) != cudaSuccess) return e;
+        e = launch_kernel(kern, grid, dim3(kThreads), kSmemBytes, s, true, tmap, p);
+    }
+    if (e != cudaSuccess || sp.splits == 1) return e;
+    const int64_t count4 = q.m * q.n / 4;
+    return launch_kernel(prefill_reduce_kernel,
+                         dim3(static_cast<unsigned>(std::min<int64_t>((count4 + 255) / 256,
+                                                                      int64_t{device_sm_count()} * 8))),
+                         dim3(256), 0, s, true, reinterpret_cast<const float4*>(part), reinterpret_cast<float4*>(q.y),
+                         count4, sp.splits);
+}
 
 }  // namespace phb
