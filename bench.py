@@ -165,7 +165,7 @@ def build_decode(seed):
                 for i, (_, n, k) in enumerate(LAYER_SHAPES)]
         layers.append(mats)
     table = phb.layer_table(layers)
-    ws = phb.workspace(phb.decode_workspace_size("q8_0", D_MODEL, N_Q, N_KV, HD, D_FF))
+    ws = phb.decode_workspace("q8_0", D_MODEL, N_Q, N_KV, HD, D_FF)
     return layers, table, ws
 
 

@@ -183,9 +183,23 @@ phb_status phb_gemm_q_prefill(int qtype, const void* W, const float* X, float* Y
  * layers: HOST array of n_layers descriptors whose members are DEVICE
  * pointers to qtype matrices: Wqkv [(n_q+2n_kv)*head_dim][d_model],
  * Wo [d_model][n_q*head_dim], Wgate/Wup [d_ff][d_model], Wdown [d_model][d_ff].
- * x_in, x_out: [d_model] fp32 (may not alias). Launches 4 kernels per layer
- * on `stream`, so the whole step can be captured in a CUDA graph by the
- * caller after one uncaptured call.
+ * x_in, x_out: [d_model] fp32 (may not alias).
+ *
+ * phb_decode_step runs the fused path: one cooperative kernel per 64 layers,
+ * one CTA per SM, in which every CTA streams its slice of all the layers'
+ * weights through one shared-memory ring while the GEMVs wait on each other
+ * through tagged intermediate vectors (with activations held in registers).
+ * Its workspace carries a call epoch: zero it before the first call and
+ * pass the same, otherwise untouched, workspace to later calls; calls
+ * sharing a workspace must not overlap on the GPU. After a device error
+ * (phb_device_error) the workspace must be zeroed again. The fused path
+ * needs 2*d_model/256 and every K/256 to be at most the stage size (176
+ * units), head_dim % 32 == 0 and ceil(d_model/SMs) <= 352; other shapes
+ * return PHB_ERR_SHAPE (use phb_decode_step_unfused).
+ * phb_decode_step_unfused launches the same arithmetic as 4 kernels per
+ * layer (the pages' "launched" path that `fuse_check` compares the fused
+ * one against); it needs no zeroing. Both can be captured in a CUDA graph
+ * after one uncaptured call.
  * ------------------------------------------------------------------------- */
 typedef struct phb_dense_layer {
     const void* w_qkv;
@@ -201,6 +215,10 @@ phb_status phb_decode_step(int qtype, const phb_dense_layer* layers, int n_layer
                            int64_t d_model, int n_q_heads, int n_kv_heads, int head_dim, int64_t d_ff,
                            const float* x_in, float* x_out,
                            void* ws, size_t ws_bytes, phb_stream_t stream);
+phb_status phb_decode_step_unfused(int qtype, const phb_dense_layer* layers, int n_layers,
+                                   int64_t d_model, int n_q_heads, int n_kv_heads, int head_dim, int64_t d_ff,
+                                   const float* x_in, float* x_out,
+                                   void* ws, size_t ws_bytes, phb_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * SwiGLU feed-forward block that allocates nothing. The paper has no

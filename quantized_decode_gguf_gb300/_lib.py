@@ -44,6 +44,8 @@ SIGNATURES = {
     "phb_decode_step_workspace_size": (_c_sz, [_c_int, _c_i64, _c_int, _c_int, _c_int, _c_i64]),
     "phb_decode_step": (_c_int, [_c_int, _c_vp, _c_int, _c_i64, _c_int, _c_int, _c_int, _c_i64, _c_vp, _c_vp, _c_vp,
                                  _c_sz, _c_vp]),
+    "phb_decode_step_unfused": (_c_int, [_c_int, _c_vp, _c_int, _c_i64, _c_int, _c_int, _c_int, _c_i64, _c_vp, _c_vp,
+                                         _c_vp, _c_sz, _c_vp]),
 }
 
 

@@ -183,15 +183,26 @@ def layer_table(layers: Sequence[Sequence[torch.Tensor]]):
     return arr
 
 
+def decode_workspace(qtype, d_model: int, n_q: int, n_kv: int, head_dim: int, d_ff: int, device=None):
+    """Zeroed workspace for :func:`decode_step` (the fused step keeps a call counter in it)."""
+    n = decode_workspace_size(qtype, d_model, n_q, n_kv, head_dim, d_ff)
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+
+
 def decode_step(qtype, table, n_layers: int, d_model: int, n_q: int, n_kv: int, head_dim: int, d_ff: int,
                 x_in: torch.Tensor, x_out: Optional[torch.Tensor] = None,
-                ws: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """One decode step; ``table`` comes from :func:`layer_table`."""
+                ws: Optional[torch.Tensor] = None, fused: bool = True) -> torch.Tensor:
+    """One decode step; ``table`` comes from :func:`layer_table`.
+
+    ``fused`` selects phb_decode_step (one cooperative kernel; ``ws`` from
+    :func:`decode_workspace`, reused across calls) or phb_decode_step_unfused.
+    """
     qt = qtype_id(qtype)
     if x_out is None:
         x_out = torch.empty_like(x_in)
     if ws is None:
-        ws = workspace(decode_workspace_size(qt, d_model, n_q, n_kv, head_dim, d_ff), x_in.device)
-    _check(_lib.load().phb_decode_step(qt, ctypes.cast(table, ctypes.c_void_p), n_layers, d_model, n_q, n_kv,
-                                       head_dim, d_ff, _ptr(x_in), _ptr(x_out), _ptr(ws), ws.numel(), _stream()))
+        ws = decode_workspace(qt, d_model, n_q, n_kv, head_dim, d_ff, x_in.device)
+    fn = _lib.load().phb_decode_step if fused else _lib.load().phb_decode_step_unfused
+    _check(fn(qt, ctypes.cast(table, ctypes.c_void_p), n_layers, d_model, n_q, n_kv, head_dim, d_ff, _ptr(x_in),
+              _ptr(x_out), _ptr(ws), ws.numel(), _stream()))
     return x_out

@@ -207,12 +207,13 @@ phb_status phb_device_error(int* code) {
     phb_status st = check_device();
     if (st != PHB_OK) return st;
     PHB_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
-    int c[4] = {0, 0, 0, 0};
+    int c[5] = {0, 0, 0, 0, 0};
     PHB_CUDA(phb::read_dev_err_gemv(&c[0]), "read device error");
     PHB_CUDA(phb::read_dev_err_decode(&c[1]), "read device error");
     PHB_CUDA(phb::read_dev_err_moe(&c[2]), "read device error");
     PHB_CUDA(phb::read_dev_err_prefill(&c[3]), "read device error");
-    *code = c[0] | c[1] | c[2] | c[3];
+    PHB_CUDA(phb::read_dev_err_decode_persistent(&c[4]), "read device error");
+    *code = c[0] | c[1] | c[2] | c[3] | c[4];
     if (*code) return fail(PHB_ERR_DEVICE_TIMEOUT, "a kernel reported device error %d", *code);
     return ok();
 }
@@ -437,13 +438,15 @@ phb_status phb_gemm_q_prefill(int qtype, const void* W, const float* X, float* Y
 size_t phb_decode_step_workspace_size(int qtype, int64_t d_model, int n_q_heads, int n_kv_heads, int head_dim,
                                       int64_t d_ff) {
     if (qt_of(qtype) < 0 || d_model <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 || d_ff <= 0) return 0;
-    return decode_ws(d_model, n_q_heads, n_kv_heads, head_dim, d_ff, nullptr).bytes;
+    const size_t unfused = decode_ws(d_model, n_q_heads, n_kv_heads, head_dim, d_ff, nullptr).bytes;
+    const size_t fused = phb::decode_persistent_ws_bytes(d_model, n_q_heads, n_kv_heads, head_dim, d_ff) +
+                         2 * align256(static_cast<size_t>(d_model) * sizeof(float));
+    return std::max(unfused, fused);
 }
 
-phb_status phb_decode_step(int qtype, const phb_dense_layer* layers, int n_layers, int64_t d_model, int n_q_heads,
-                           int n_kv_heads, int head_dim, int64_t d_ff, const float* x_in, float* x_out, void* ws,
-                           size_t ws_bytes, phb_stream_t stream) {
-    const int qt = qt_of(qtype);
+static phb_status validate_decode(int qt, const phb_dense_layer* layers, int n_layers, int64_t d_model, int n_q_heads,
+                                  int n_kv_heads, int head_dim, int64_t d_ff, const float* x_in, float* x_out,
+                                  void* ws, size_t ws_bytes) {
     PHB_REQUIRE(qt >= 0, PHB_ERR_INVALID_ARG, "unknown qtype");
     PHB_REQUIRE(layers && x_in && x_out, PHB_ERR_INVALID_ARG, "null pointer");
     PHB_REQUIRE(n_layers >= 1, PHB_ERR_INVALID_ARG, "n_layers must be positive");
@@ -463,11 +466,60 @@ phb_status phb_decode_step(int qtype, const phb_dense_layer* layers, int n_layer
                         aligned16(L.w_down),
                     PHB_ERR_ALIGN, "layer %d: weights must be 16-byte aligned", l);
     }
-    const size_t need = decode_ws(d_model, n_q_heads, n_kv_heads, head_dim, d_ff, nullptr).bytes;
+    const size_t need = phb_decode_step_workspace_size(qt == 0 ? PHB_Q8_0 : PHB_Q4_K, d_model, n_q_heads, n_kv_heads,
+                                                       head_dim, d_ff);
     PHB_REQUIRE(ws && ws_bytes >= need, PHB_ERR_WORKSPACE, "workspace needs %zu bytes (got %zu)", need, ws_bytes);
-    phb_status st = check_device();
+    return PHB_OK;
+}
+
+phb_status phb_decode_step(int qtype, const phb_dense_layer* layers, int n_layers, int64_t d_model, int n_q_heads,
+                           int n_kv_heads, int head_dim, int64_t d_ff, const float* x_in, float* x_out, void* ws,
+                           size_t ws_bytes, phb_stream_t stream) {
+    const int qt = qt_of(qtype);
+    phb_status st = validate_decode(qt, layers, n_layers, d_model, n_q_heads, n_kv_heads, head_dim, d_ff, x_in, x_out,
+                                    ws, ws_bytes);
+    if (st != PHB_OK) return st;
+    st = check_device();
+    if (st != PHB_OK) return st;
+    // one cooperative kernel per chunk of at most kPersistMaxLayers layers; the
+    // chunks hand the residual stream over through two plain buffers at the
+    // end of the workspace
+    auto* base = static_cast<uint8_t*>(ws);
+    const size_t pbytes = phb::decode_persistent_ws_bytes(d_model, n_q_heads, n_kv_heads, head_dim, d_ff);
+    float* hand[2] = {reinterpret_cast<float*>(base + pbytes),
+                      reinterpret_cast<float*>(base + pbytes + align256(static_cast<size_t>(d_model) * sizeof(float)))};
+    const void* wl[5 * phb::kPersistMaxLayers];
+    for (int l0 = 0, chunk = 0; l0 < n_layers; l0 += phb::kPersistMaxLayers, ++chunk) {
+        const int nl = std::min(phb::kPersistMaxLayers, n_layers - l0);
+        for (int l = 0; l < nl; ++l) {
+            const phb_dense_layer& L = layers[l0 + l];
+            wl[5 * l] = L.w_qkv;
+            wl[5 * l + 1] = L.w_o;
+            wl[5 * l + 2] = L.w_gate;
+            wl[5 * l + 3] = L.w_up;
+            wl[5 * l + 4] = L.w_down;
+        }
+        const float* in = l0 == 0 ? x_in : hand[(chunk - 1) & 1];
+        float* out = l0 + nl == n_layers ? x_out : hand[chunk & 1];
+        const cudaError_t e = phb::decode_persistent_run(qt, wl, nl, d_model, n_q_heads, n_kv_heads, head_dim, d_ff,
+                                                         in, out, ws, stream);
+        if (e == cudaErrorInvalidConfiguration) return fail(PHB_ERR_SHAPE, "shape does not fit the persistent decode kernel");
+        if (e != cudaSuccess) return cuda_fail(e, "persistent decode launch");
+    }
+    return ok();
+}
+
+phb_status phb_decode_step_unfused(int qtype, const phb_dense_layer* layers, int n_layers, int64_t d_model,
+                                   int n_q_heads, int n_kv_heads, int head_dim, int64_t d_ff, const float* x_in,
+                                   float* x_out, void* ws, size_t ws_bytes, phb_stream_t stream) {
+    const int qt = qt_of(qtype);
+    phb_status st = validate_decode(qt, layers, n_layers, d_model, n_q_heads, n_kv_heads, head_dim, d_ff, x_in, x_out,
+                                    ws, ws_bytes);
+    if (st != PHB_OK) return st;
+    st = check_device();
     if (st != PHB_OK) return st;
     const DecodeWs w = decode_ws(d_model, n_q_heads, n_kv_heads, head_dim, d_ff, ws);
+    const int64_t q_dim = static_cast<int64_t>(n_q_heads) * head_dim;
     const int64_t qkv_dim = static_cast<int64_t>(n_q_heads + 2 * n_kv_heads) * head_dim;
     // GEMV launch ids for debug tracing builds. (Prefetching the weights of
     // GEMV i + 2 into L2 from GEMV i measured slightly slower here, so the

@@ -96,6 +96,44 @@ __device__ __forceinline__ void dot_q8_0_half(const uint8_t* wsrc, const float* 
     }
 }
 
+// dot_q8_0_half for one activation row held in registers: xr the half
+// unit's 128 scaled activations, xsr its four unscaled 32-sums. A thread that
+// keeps xr across many rows reads only weights from shared memory. Same
+// arithmetic, in the same order, as dot_q8_0_half with MAXB = 1.
+__device__ __forceinline__ float dot_q8_0_half_xr(const uint8_t* wsrc, const float (&xr)[128], const float (&xsr)[4],
+                                                  float xfac) {
+    uint32_t wd[34];
+#pragma unroll
+    for (int i = 0; i < 17; ++i) {
+        const uint2 v = *reinterpret_cast<const uint2*>(wsrc + 8 * i);
+        wd[2 * i] = v.x;
+        wd[2 * i + 1] = v.y;
+    }
+    float acc = 0.f;
+#pragma unroll
+    for (int bb = 0; bb < 4; ++bb) {
+        const int ob = 34 * bb;
+        const float d = fp16_bits_to_float((ob % 4) ? (wd[ob / 4] >> 16) : wd[ob / 4]);
+        float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int i4 = 0; i4 < 8; ++i4) {
+            float q[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const int p = ob + 2 + 4 * i4 + t;
+                q[t] = byte_subnormal_rt(wd[p / 4] ^ 0x80808080u, p % 4);
+            }
+            const int k = 32 * bb + 4 * i4;
+            s2 = ffma2(q[0], q[1], xr[k], xr[k + 1], s2);
+            s2 = ffma2(q[2], q[3], xr[k + 2], xr[k + 3], s2);
+        }
+        const float su = s2.x + s2.y;
+        const float blk = fmaf(su, xfac, -128.f * xsr[bb]);
+        acc = fmaf(d, blk, acc);
+    }
+    return acc;
+}
+
 // 6-bit scale and min of sub-block 4h + jj from the 12 scale bytes (packed
 // little-endian in sw[0..2]); branch-free in h.
 __device__ __forceinline__ void q4_k_scale_min_half(const uint32_t (&sw)[3], int h, int jj, uint32_t& sc, uint32_t& m) {
@@ -170,6 +208,53 @@ __device__ __forceinline__ void dot_q4_k_half(const uint8_t* blk, int h, const f
             acc[b] = fmaf(-mh, xsum[b * sstride + 2 * cc + 1], acc[b]);
         }
     }
+}
+
+// dot_q4_k_half for one activation row held in registers (see
+// dot_q8_0_half_xr); same arithmetic, in the same order, as MAXB = 1.
+__device__ __forceinline__ float dot_q4_k_half_xr(const uint8_t* blk, int h, const float (&xr)[128],
+                                                  const float (&xsr)[4], float xfac) {
+    const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
+    const float d = fp16_bits_to_float(hdr.x);
+    const float dmin = fp16_bits_to_float(hdr.x >> 16);
+    const uint32_t sw[3] = {hdr.y, hdr.z, hdr.w};
+    uint32_t qw[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint4 v = *reinterpret_cast<const uint4*>(blk + 16 + 64 * h + 16 * i);
+        qw[4 * i] = v.x;
+        qw[4 * i + 1] = v.y;
+        qw[4 * i + 2] = v.z;
+        qw[4 * i + 3] = v.w;
+    }
+    float acc = 0.f;
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+        float2 slo = make_float2(0.f, 0.f), shi = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int wi = 0; wi < 8; ++wi) {
+            const uint32_t w = qw[8 * cc + wi];
+            const uint32_t lo = w & 0x0F0F0F0Fu;
+            const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;
+            const int kl = 64 * cc + 4 * wi, kh = kl + 32;
+            slo = ffma2(byte_subnormal<0>(lo), byte_subnormal<1>(lo), xr[kl], xr[kl + 1], slo);
+            slo = ffma2(byte_subnormal<2>(lo), byte_subnormal<3>(lo), xr[kl + 2], xr[kl + 3], slo);
+            shi = ffma2(byte_subnormal<0>(hi), byte_subnormal<1>(hi), xr[kh], xr[kh + 1], shi);
+            shi = ffma2(byte_subnormal<2>(hi), byte_subnormal<3>(hi), xr[kh + 2], xr[kh + 3], shi);
+        }
+        uint32_t sc_l, m_l, sc_h, m_h;
+        q4_k_scale_min_half(sw, h, 2 * cc, sc_l, m_l);
+        q4_k_scale_min_half(sw, h, 2 * cc + 1, sc_h, m_h);
+        const float dl = d * static_cast<float>(sc_l), ml = dmin * static_cast<float>(m_l);
+        const float dh = d * static_cast<float>(sc_h), mh = dmin * static_cast<float>(m_h);
+        const float ql = (slo.x + slo.y) * xfac;
+        const float qh = (shi.x + shi.y) * xfac;
+        acc = fmaf(dl, ql, acc);
+        acc = fmaf(-ml, xsr[2 * cc], acc);
+        acc = fmaf(dh, qh, acc);
+        acc = fmaf(-mh, xsr[2 * cc + 1], acc);
+    }
+    return acc;
 }
 
 }  // namespace phb

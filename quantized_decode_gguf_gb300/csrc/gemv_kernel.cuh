@@ -38,7 +38,7 @@ static __device__ int g_dev_err;
 
 #ifdef PHB_TRACE
 // Debug builds only: per-CTA timestamps [launch id][cta][event].
-constexpr int kTraceLaunches = 128, kTraceCtas = 160, kTraceEvents = 6;
+constexpr int kTraceLaunches = 128, kTraceCtas = 160, kTraceEvents = 8;
 static __device__ uint64_t g_trace[kTraceLaunches * kTraceCtas * kTraceEvents];
 #define PHB_TRACE_EV(id, ev)                                                                          \
     do {                                                                                              \
@@ -51,6 +51,12 @@ static __device__ uint64_t g_trace[kTraceLaunches * kTraceCtas * kTraceEvents];
     } while (0)
 #endif
 
+#ifndef PHB_STAGE_HOOK
+#define PHB_STAGE_HOOK(kind, s) \
+    do {                        \
+    } while (0)
+#endif
+
 enum XMode : int { kXPlain = 0, kXRmsNorm = 1, kXGatherV = 2, kXRowList = 3 };
 enum Epi : int { kEpiStore = 0, kEpiResid = 1, kEpiSwiGLU = 2 };
 enum RowSum : int { kSumWarp = 0, kSumTile = 1, kSumFold = 2 };
@@ -60,16 +66,16 @@ constexpr float kRmsEps = 1e-6f;
 constexpr int kMaxConsumerWarps = 16;
 
 // Per-configuration constants: QT format, CW consumer warps.
-template <int QT, int CW>
+template <int QT, int CW, int NS = (QT == 0 ? 2 : 3)>
 struct KCfg {
     static constexpr int consumers = 32 * CW;
     static constexpr int threads = consumers + 32;    // + one producer warp
     static constexpr int stage_units = consumers / 2; // one half unit per consumer thread
     static constexpr int ub = Fmt<QT>::unit_bytes;
     static constexpr int stage_bytes = stage_units * ub;
-    // ring depth: 70 KB of Q8_0 or 55 KB of Q4_K at 8 warps, so that two
-    // CTAs (this kernel's and the next one's) fit on an SM
-    static constexpr int ns = QT == 0 ? 2 : 3;
+    // ring depth; the default (70 KB of Q8_0 or 55 KB of Q4_K at 8 warps)
+    // lets two CTAs (this kernel's and the next one's) share an SM
+    static constexpr int ns = NS;
 };
 
 // Floats after the mbarriers: xfac [kAccStride], reduction scratch
@@ -111,17 +117,19 @@ __device__ __forceinline__ void prefetch_share(const uint8_t* p, int64_t bytes) 
 // Producer: stream the tile's unit list through the stage ring, continuing
 // the ring position `s` (a stage counter shared with the consumers).
 // Returns false on a wait timeout.
-template <int QT, int CW>
+template <int QT, int CW, int NS = KCfg<QT, CW>::ns>
 __device__ __forceinline__ bool produce_tile(const Tile& t, int nmat, uint8_t* stages, uint64_t* full,
-                                             uint64_t* empty, int& s, uint64_t pol) {
-    using C = KCfg<QT, CW>;
+                                             uint64_t* empty, int& s, uint64_t pol,
+                                             int stage_units = KCfg<QT, CW, NS>::stage_units) {
+    using C = KCfg<QT, CW, NS>;
     const int units = nmat * t.rows_here * t.useg;
     // with one matrix and whole rows the list is one contiguous byte range
     const bool flat = (nmat == 1) && t.contiguous;
-    for (int g0 = 0; g0 < units; g0 += C::stage_units, ++s) {
+    for (int g0 = 0; g0 < units; g0 += stage_units, ++s) {
         const int slot = s % C::ns;
         if (s >= C::ns && !mbar_wait(&empty[slot], ((s / C::ns) - 1) & 1, &g_dev_err)) return false;
-        const int g1 = min(units, g0 + C::stage_units);
+        const int g1 = min(units, g0 + stage_units);
+        PHB_STAGE_HOOK(0, s);
         mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>((g1 - g0) * C::ub));
         uint8_t* dst = stages + slot * C::stage_bytes;
         if (flat) {
@@ -151,12 +159,12 @@ __device__ __forceinline__ bool produce_tile(const Tile& t, int nmat, uint8_t* s
 // 2 * units * MAXB floats for kSumTile, MAXB * consumers for kSumFold;
 // `row_acc` NMAT * rows_here * kAccStride floats (kSumFold; zeroed by the
 // caller before its last consumer barrier). Returns false on a wait timeout.
-template <int QT, int CW, int MAXB, int NMAT, class EpiF>
+template <int QT, int CW, int MAXB, int NMAT, int NS = KCfg<QT, CW>::ns, class EpiF>
 __device__ __forceinline__ bool consume_tile(const Tile& t, int mode, const uint8_t* stages, uint64_t* full,
                                              uint64_t* empty, int& s, const float* xs, int xstride,
                                              const float* xsum, int sstride, const float* xfac, int batch,
                                              float* part, float* row_acc, EpiF epi) {
-    using C = KCfg<QT, CW>;
+    using C = KCfg<QT, CW, NS>;
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int hsel = tid & 1;
@@ -165,10 +173,12 @@ __device__ __forceinline__ bool consume_tile(const Tile& t, int mode, const uint
     const int seg_half = 2 * t.useg;  // half units per row segment
     for (int g0 = 0; g0 < units; g0 += C::stage_units, ++s) {
         const int slot = s % C::ns;
+        if (threadIdx.x == 0) PHB_STAGE_HOOK(2, s);
         if (!mbar_wait_warp(&full[slot], (s / C::ns) & 1, &g_dev_err)) {
             mbar_wait(&full[slot], (s / C::ns) & 1, &g_dev_err);  // second bounded wait for the copy in flight
             return false;
         }
+        if (threadIdx.x == 0) PHB_STAGE_HOOK(1, s);
         const int g = g0 + ulocal;
         const int segi = g / t.useg;
         const int u = g - segi * t.useg;

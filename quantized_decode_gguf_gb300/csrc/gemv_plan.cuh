@@ -51,11 +51,12 @@ constexpr size_t kTilePartBudget = 48 * 1024;
 // decode GEMVs (a 24-layer Q8_0 step: 550 us with 2, 775 us with 1).
 constexpr int kCtasPerSm = PHB_CTAS_PER_SM;
 
-inline SmemLayout stream_smem_layout(int qt, int cw, int nmat, int maxb, int rows_per_cta, int units_seg) {
+inline SmemLayout stream_smem_layout(int qt, int cw, int nmat, int maxb, int rows_per_cta, int units_seg,
+                                     int ring_stages = 0) {
     const int ub = qt == 0 ? Fmt<0>::unit_bytes : Fmt<1>::unit_bytes;
     const int consumers = 32 * cw;
     const int stage_units = consumers / 2;
-    const int ns = qt == 0 ? 2 : 3;
+    const int ns = ring_stages > 0 ? ring_stages : (qt == 0 ? KCfg<0, 8>::ns : KCfg<1, 8>::ns);
     SmemLayout l{};
     size_t off = static_cast<size_t>(ns) * stage_units * ub;
     const size_t kseg = static_cast<size_t>(units_seg) * kUnitWeights;

@@ -97,6 +97,14 @@ cudaError_t swiglu_run(const float* g, const float* u, float* h, int64_t count, 
 // ---------------------------------------------------------------- decode step
 cudaError_t decode_gemv_run(const GemvReq& q, cudaStream_t s);  // rmsnorm / gather / residual variants
 
+// Persistent (one cooperative kernel) decode step over at most kPersistMaxLayers
+// layers; wl holds 5 weight pointers per layer (qkv, o, gate, up, down); ws
+// is decode_persistent_ws_bytes long and zeroed before its first use.
+constexpr int kPersistMaxLayers = 64;
+size_t decode_persistent_ws_bytes(int64_t d_model, int n_q, int n_kv, int hd, int64_t d_ff);
+cudaError_t decode_persistent_run(int qt, const void* const* wl, int n_layers, int64_t d_model, int n_q, int n_kv,
+                                  int hd, int64_t d_ff, const float* x_in, float* x_out, void* ws, cudaStream_t s);
+
 // ---------------------------------------------------------------- dequant
 cudaError_t dequant_run(int qt, bool bf16, const void* blocks, void* w, int64_t n, int64_t k, cudaStream_t s);
 
@@ -137,5 +145,6 @@ cudaError_t read_dev_err_gemv(int* code);
 cudaError_t read_dev_err_decode(int* code);
 cudaError_t read_dev_err_moe(int* code);
 cudaError_t read_dev_err_prefill(int* code);
+cudaError_t read_dev_err_decode_persistent(int* code);
 
 }  // namespace phb

@@ -170,15 +170,59 @@ def _deq_layer(qtype, blobs):
     return [oracle.dequant(qtype, b, r, c) for b, (r, c) in zip(blobs, shapes)]
 
 
+@pytest.mark.parametrize("fused", [True, False])
 @pytest.mark.parametrize("qtype", ["q8_0", "q4_k"])
-def test_decode_single_layer_within_bound(qtype):
+def test_decode_single_layer_within_bound(qtype, fused):
     blobs = _layer_blobs(qtype, 600, 0)
     dev = [to_dev(b) for b in blobs]
     table = phb.layer_table([dev])
     x = synth.normal_f32(600, 999, (D_MODEL,))
-    y = to_host(phb.decode_step(qtype, table, 1, D_MODEL, N_Q, N_KV, HD, D_FF, to_dev(x)))
+    y = to_host(phb.decode_step(qtype, table, 1, D_MODEL, N_Q, N_KV, HD, D_FF, to_dev(x), fused=fused))
     ref, bound = oracle.decode_layer(x, np.zeros((1, D_MODEL)), *_deq_layer(qtype, blobs), N_Q, N_KV, HD)
-    assert_within(y[None, :], ref, bound, f"decode layer {qtype}")
+    assert_within(y[None, :], ref, bound, f"decode layer {qtype} fused={fused}")
+    check_device_clean()
+
+
+@pytest.mark.parametrize("qtype", ["q8_0", "q4_k"])
+def test_fused_decode_matches_launched_decode(qtype):
+    # the pages' fuse_check: the fused decode path against the launched one,
+    # here over 4 layers and 5 calls through one workspace (the fused step's
+    # tag epoch advances across calls and graph replays)
+    n_layers = 4
+    dev = [[to_dev(b) for b in _layer_blobs(qtype, 610, l)] for l in range(n_layers)]
+    table = phb.layer_table(dev)
+    ws = phb.decode_workspace(qtype, D_MODEL, N_Q, N_KV, HD, D_FF)
+    for call in range(5):
+        x = to_dev(synth.normal_f32(610, 1000 + call, (D_MODEL,)))
+        yf = to_host(phb.decode_step(qtype, table, n_layers, D_MODEL, N_Q, N_KV, HD, D_FF, x, ws=ws))
+        yu = to_host(phb.decode_step(qtype, table, n_layers, D_MODEL, N_Q, N_KV, HD, D_FF, x, fused=False))
+        scale = np.abs(yu).max()
+        assert np.all(np.abs(yf - yu) <= 1e-5 * scale), (call, np.abs(yf - yu).max() / scale)
+    check_device_clean()
+
+
+def test_fused_decode_in_a_cuda_graph_replays():
+    qtype, n_layers = "q8_0", 2
+    dev = [[to_dev(b) for b in _layer_blobs(qtype, 620, l)] for l in range(n_layers)]
+    table = phb.layer_table(dev)
+    ws = phb.decode_workspace(qtype, D_MODEL, N_Q, N_KV, HD, D_FF)
+    x = to_dev(synth.normal_f32(620, 1, (D_MODEL,)))
+    y = torch.empty_like(x)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        phb.decode_step(qtype, table, n_layers, D_MODEL, N_Q, N_KV, HD, D_FF, x, y, ws)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        phb.decode_step(qtype, table, n_layers, D_MODEL, N_Q, N_KV, HD, D_FF, x, y, ws)
+    ref = to_host(phb.decode_step(qtype, table, n_layers, D_MODEL, N_Q, N_KV, HD, D_FF, x, fused=False))
+    for i in range(4):
+        x.copy_(to_dev(synth.normal_f32(620, 10 + i, (D_MODEL,))))
+        g.replay()
+        want = to_host(phb.decode_step(qtype, table, n_layers, D_MODEL, N_Q, N_KV, HD, D_FF, x, fused=False))
+        got = to_host(y)
+        assert np.all(np.abs(got - want) <= 1e-5 * np.abs(want).max()), i
+    assert ref is not None
     check_device_clean()
 
 
