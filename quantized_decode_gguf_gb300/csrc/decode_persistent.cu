@@ -100,17 +100,20 @@ __device__ __forceinline__ unsigned ld_relaxed(const unsigned* p) {
     return v;
 }
 
-__device__ __forceinline__ uint4 ld_l2_u4(const void* p) {
-    uint4 v;
-    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p)
-                 : "memory");
-    return v;
+// Tagged pairs are moved as single 64-bit accesses ({value, tag} in the low
+// and high word), which the memory model makes single-copy atomic: a reader
+// never sees the tag of one store with the value of another.
+__device__ __forceinline__ void ld_l2_pairs2(const uint2* p, uint2& a, uint2& b) {
+    unsigned long long u, v;
+    asm volatile("ld.global.cg.v2.u64 {%0, %1}, [%2];" : "=l"(u), "=l"(v) : "l"(p) : "memory");
+    a = make_uint2(static_cast<unsigned>(u), static_cast<unsigned>(u >> 32));
+    b = make_uint2(static_cast<unsigned>(v), static_cast<unsigned>(v >> 32));
 }
 
-__device__ __forceinline__ uint2 ld_l2_u2(const void* p) {
-    uint2 v;
-    asm volatile("ld.global.cg.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p) : "memory");
-    return v;
+__device__ __forceinline__ uint2 ld_l2_pair(const uint2* p) {
+    unsigned long long u;
+    asm volatile("ld.global.cg.u64 %0, [%1];" : "=l"(u) : "l"(p) : "memory");
+    return make_uint2(static_cast<unsigned>(u), static_cast<unsigned>(u >> 32));
 }
 
 __device__ __forceinline__ float4 ld_l2_f4(const float* p) {
@@ -121,14 +124,17 @@ __device__ __forceinline__ float4 ld_l2_f4(const float* p) {
 }
 
 __device__ __forceinline__ void st_pair(uint2* p, float v, unsigned tag) {
-    asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(__float_as_uint(v)), "r"(tag) : "memory");
+    const unsigned long long u = static_cast<unsigned long long>(tag) << 32 | __float_as_uint(v);
+    asm volatile("st.global.u64 [%0], %1;" ::"l"(p), "l"(u) : "memory");
 }
 
 // Four consecutive tagged values starting at pair e; true when all carry tag.
 __device__ __forceinline__ bool ld_tagged4(const uint2* src, int e, unsigned tag, float4& v) {
-    const uint4 a = ld_l2_u4(src + e), b = ld_l2_u4(src + e + 2);
-    v = make_float4(__uint_as_float(a.x), __uint_as_float(a.z), __uint_as_float(b.x), __uint_as_float(b.z));
-    return a.y == tag && a.w == tag && b.y == tag && b.w == tag;
+    uint2 a, b, c, d;
+    ld_l2_pairs2(src + e, a, b);
+    ld_l2_pairs2(src + e + 2, c, d);
+    v = make_float4(__uint_as_float(a.x), __uint_as_float(b.x), __uint_as_float(c.x), __uint_as_float(d.x));
+    return a.y == tag && b.y == tag && c.y == tag && d.y == tag;
 }
 
 __device__ __forceinline__ void set_abort(unsigned* state) {
@@ -201,8 +207,9 @@ template <int XMODE>
 __device__ __forceinline__ bool stage_vec(const PersistParams& p, const uint2* src_t, const float* src_p, unsigned tag,
                                           int kseg, float* xs, float* xsum, float* xfac, float* red, int* flag,
                                           const uint2* res_t, const float* res_p, unsigned res_tag, float* res_dst,
-                                          int nres, int trace_op) {
+                                          int nres, int* retries, int trace_op) {
     (void)trace_op;
+    (void)retries;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n4 = kseg / 4;  // a multiple of 64
     bool ok = true;
@@ -212,7 +219,7 @@ __device__ __forceinline__ bool stage_vec(const PersistParams& p, const uint2* s
         if (res_p != nullptr)
             ra.x = __float_as_uint(res_p[tid]);
         else
-            ra = ld_l2_u2(res_t + tid);
+            ra = ld_l2_pair(res_t + tid);
     }
     float ssq = 0.f, mx = 0.f;
     // XMODE 2 reads only the n_kv V heads (group query heads share each) and
@@ -234,6 +241,14 @@ __device__ __forceinline__ bool stage_vec(const PersistParams& p, const uint2* s
                     miss |= 1u << i;
             }
         }
+#ifdef PHB_TRACE
+        if (tid == 0 && base == 0) {
+            float chk = v[0].x;  // wait for the first pass's data
+            asm volatile("" ::"f"(chk));
+            if (miss == 0) PHB_TRACE_EV(trace_op, 8);
+        }
+        if (miss != 0 && retries != nullptr) atomicAdd(retries, 1);
+#endif
         if (miss != 0) {
             // some pairs were not yet current: re-read those (bounded)
             WaitClock clk;
@@ -287,7 +302,7 @@ __device__ __forceinline__ bool stage_vec(const PersistParams& p, const uint2* s
                 break;
             }
             __nanosleep(32);
-            ra = ld_l2_u2(res_t + tid);
+            ra = ld_l2_pair(res_t + tid);
         }
         res_dst[tid] = __uint_as_float(ra.x);
     }
@@ -303,25 +318,26 @@ __device__ __forceinline__ bool stage_vec(const PersistParams& p, const uint2* s
         red[kCW + warp] = ssq;
     }
     consumer_sync<kNC>();
-    if (tid == 0) PHB_TRACE_EV(trace_op, 5);
-    float* sc = red + 2 * kCW;  // [0] r, [1] f1, [2] f2
+#ifdef PHB_TRACE
     if (tid == 0) {
-        float m = 0.f, q = 0.f;
-        for (int w = 0; w < kCW; ++w) {
-            m = fmaxf(m, red[w]);
-            q += red[kCW + w];
-        }
-        const float r = XMODE == 1 ? rsqrtf(q / static_cast<float>(kseg) + kRmsEps) : 1.f;
-        const int se = pick_scale_exp(m * r);
-        const int e1 = min(se, 127);
-        sc[0] = r;
-        sc[1] = ldexpf(1.0f, e1);
-        sc[2] = ldexpf(1.0f, se - e1);
-        xfac[0] = ldexpf(1.0f, 149 - se);
+        if (trace_op < kTraceLaunches && blockIdx.x < kTraceCtas)
+            g_trace[(trace_op * kTraceCtas + blockIdx.x) * kTraceEvents + 9] = static_cast<uint64_t>(*retries);
+        *retries = 0;
     }
-    consumer_sync<kNC>();
+#endif
+    if (tid == 0) PHB_TRACE_EV(trace_op, 5);
+    // every thread derives the same scale from the per-warp partials
+    float m = 0.f, sq = 0.f;
+    for (int w = 0; w < kCW; ++w) {
+        m = fmaxf(m, red[w]);
+        sq += red[kCW + w];
+    }
+    const float r = XMODE == 1 ? rsqrtf(sq / static_cast<float>(kseg) + kRmsEps) : 1.f;
+    const int se = pick_scale_exp(m * r);
+    const int e1 = min(se, 127);
+    const float f1 = __int_as_float((e1 + 127) << 23), f2 = __int_as_float((se - e1 + 127) << 23);
+    if (tid == 0) xfac[0] = __int_as_float((149 - se + 127) << 23);
     const bool all_ok = *flag == 0;
-    const float r = sc[0], f1 = sc[1], f2 = sc[2];
     for (int k4 = tid; k4 < n4; k4 += kNC) {
         float4* q = reinterpret_cast<float4*>(xs + xpad_idx(4 * k4));
         float4 v = *q;
@@ -432,6 +448,11 @@ __global__ void __launch_bounds__(KCfg<QT, kCW>::threads, 1) decode_persistent_k
     float* xfac = reinterpret_cast<float*>(empty + C::ns);
     float* red = xfac + kAccStride;
     int* flag = reinterpret_cast<int*>(red + (2 * kMaxConsumerWarps + 3) * kAccStride);
+#ifdef PHB_TRACE
+    int* retries = flag + 1;  // debug builds: re-read rounds of the staging pass
+#else
+    int* retries = nullptr;
+#endif
 
     const int tid = threadIdx.x;
     const int nctas = gridDim.x;
@@ -443,6 +464,7 @@ __global__ void __launch_bounds__(KCfg<QT, kCW>::threads, 1) decode_persistent_k
         }
         fence_barrier_init();
         *flag = 0;
+        if (retries != nullptr) *retries = 0;
     }
     __syncthreads();
     const unsigned epoch = ld_relaxed(p.state + 2);
@@ -521,21 +543,21 @@ __global__ void __launch_bounds__(KCfg<QT, kCW>::threads, 1) decode_persistent_k
             switch (j) {
                 case 0:
                     ok = stage_vec<1>(p, lin_t, lin_p, tag_lin, kseg, xs, xsum, xfac, red, flag, nullptr, nullptr, 0,
-                                      res, 0, op);
+                                      res, 0, retries, op);
                     break;
                 case 1:
                     ok = stage_vec<2>(p, p.qkv + rep * p.rs_qkv, nullptr, tag_prev, kseg, xs, xsum, xfac, red, flag,
                                       lin_t ? lin_t + row0 : nullptr, lin_p ? lin_p + row0 : nullptr, tag_lin, res,
-                                      t.rows_here, op);
+                                      t.rows_here, retries, op);
                     break;
                 case 2:
                     ok = stage_vec<1>(p, p.x1 + rep * p.rs_dm, nullptr, tag_prev, kseg, xs, xsum, xfac, red, flag, nullptr, nullptr, 0,
-                                      res, 0, op);
+                                      res, 0, retries, op);
                     break;
                 default:
                     ok = stage_vec<0>(p, p.act + rep * p.rs_ff, nullptr, tag_prev, kseg, xs, xsum, xfac, red, flag,
                                       p.x1 + rep * p.rs_dm + row0,
-                                      nullptr, tag_me - 2, res, t.rows_here, op);
+                                      nullptr, tag_me - 2, res, t.rows_here, retries, op);
                     break;
             }
             alive = ok;

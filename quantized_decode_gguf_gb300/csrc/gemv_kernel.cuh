@@ -38,7 +38,7 @@ static __device__ int g_dev_err;
 
 #ifdef PHB_TRACE
 // Debug builds only: per-CTA timestamps [launch id][cta][event].
-constexpr int kTraceLaunches = 128, kTraceCtas = 160, kTraceEvents = 8;
+constexpr int kTraceLaunches = 128, kTraceCtas = 160, kTraceEvents = 10;
 static __device__ uint64_t g_trace[kTraceLaunches * kTraceCtas * kTraceEvents];
 #define PHB_TRACE_EV(id, ev)                                                                          \
     do {                                                                                              \
@@ -288,10 +288,13 @@ __device__ __forceinline__ bool consume_tile(const Tile& t, int mode, const uint
 // (kXRmsNorm; rows are whole). s_b is chosen from max|a| so that
 // |a| * 2^s_b < 2^125. One global read pass, three consumer barriers.
 // `red` needs (2 * CW + 3) * kAccStride floats.
+// Capped at 254 so that 2^s splits into two finite factors 2^min(s,127) and
+// 2^(s-127) and 2^(149-s) stays a normal number (vectors whose largest
+// magnitude is below 2^-129 are scaled by 2^254, still below 2^125).
 __device__ __forceinline__ int pick_scale_exp(float amax) {
     if (!(amax > 0.f) || !isfinite(amax)) return 125;
     const int e = ilogbf(amax) + 1;  // amax < 2^e
-    return min(270, max(22, 125 - e));
+    return min(254, max(22, 125 - e));
 }
 
 template <int CW, int MAXB, int XMODE>

@@ -88,6 +88,25 @@ def test_gemv_within_contract(qtype, n, k, batch):
     check_device_clean()
 
 
+@pytest.mark.parametrize("qtype", ["q8_0", "q4_k"])
+def test_gemv_extreme_activation_magnitudes(qtype):
+    # per-row power-of-two staging scale at its limits: a row whose largest
+    # magnitude is below 2^-129 (scale capped at 2^254), a row near 1e30 and
+    # an all-zero row, in one batch
+    n, k = 300, 2048
+    blob = synth.blocks(qtype, 210, n, n, k)
+    x = synth.normal_f32(210, 1, (3, k))
+    x[0] *= np.float32(1e-40)
+    x[1] *= np.float32(1e30)
+    x[2] = 0.0
+    y = to_host(phb.gemv(qtype, to_dev(blob), to_dev(x), n, k))
+    ref, s = oracle.gemv_quant(qtype, blob, x, n, k)
+    assert np.all(np.isfinite(y))
+    assert_within(y, ref, 1e-3 * s + 1e-44, f"gemv {qtype} extreme magnitudes")
+    assert np.all(y[2] == 0.0)
+    check_device_clean()
+
+
 @pytest.mark.parametrize("qtype,n,k", [("q8_0", 333, 2048), ("q8_0", 40, 2048 + 32), ("q4_k", 500, 2560),
                                        ("q4_k", 64, 9728)])
 def test_gemv_unit_vectors_bit_exact(qtype, n, k):
