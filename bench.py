@@ -39,6 +39,10 @@ import synth  # noqa: E402
 
 METRIC = "Q8_0/Q4_K dequant-GEMV GB/s (% of HBM peak); batch-1 decode tok/s per model"
 D_MODEL, N_Q, N_KV, HD, D_FF, N_LAYERS = 2048, 16, 4, 128, 5632, 24
+# DRAM bytes (read + write) per launch of the fused decode kernel at 24
+# layers: an ncu capture of the 4-layer case (191.76 MB read + 3.35 MB
+# written) scaled by 6; the weights are read once per step.
+DECODE_TRAFFIC_PER_LAUNCH = 6 * (191.76e6 + 3.35e6)
 QKV = (N_Q + 2 * N_KV) * HD
 LAYER_SHAPES = [("qkv", QKV, D_MODEL), ("o", D_MODEL, N_Q * HD), ("gate", D_FF, D_MODEL), ("up", D_FF, D_MODEL),
                 ("down", D_MODEL, D_FF)]
@@ -391,6 +395,42 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+# ----------------------------------------------------------------------------- profiling runs
+
+def run_profile(args):
+    """One path only, on a small case, for ncu: --warmup untimed calls then --steps calls."""
+    import torch
+    import quantized_decode_gguf_gb300 as phb
+    seed = synth.workload_seed(1)
+    if args.profile in ("decode", "decode-unfused"):
+        n_layers = args.layers
+        layers = [[torch.from_numpy(synth.q8_0_blocks(seed, 5 * layer + i, n, k)).cuda()
+                   for i, (_, n, k) in enumerate(LAYER_SHAPES)] for layer in range(n_layers)]
+        table = phb.layer_table(layers)
+        ws = phb.decode_workspace("q8_0", D_MODEL, N_Q, N_KV, HD, D_FF)
+        x = torch.from_numpy(synth.normal_f32(seed, 100_000, (D_MODEL,))).cuda()
+        y = torch.empty_like(x)
+        fused = args.profile == "decode"
+        call = lambda: phb.decode_step("q8_0", table, n_layers, D_MODEL, N_Q, N_KV, HD, D_FF, x, y, ws,  # noqa: E731
+                                       fused=fused)
+        what = f"{'fused' if fused else 'launched'} decode step, {n_layers} layers"
+    else:
+        n, k, m = 9728, 2560, 512
+        w = torch.from_numpy(synth.blocks("q4_k", seed, 0, n, k)).cuda()
+        x = torch.from_numpy(synth.normal_f32(seed, 1, (m, k))).cuda()
+        y = torch.empty((m, n), device="cuda")
+        ws = phb.workspace(phb.prefill_workspace_size("q4_k", m, n, k))
+        call = lambda: phb.gemm_q_prefill("q4_k", w, x, n, k, out=y, ws=ws)  # noqa: E731
+        what = f"prefill GEMM Q4_K {m}x{n}x{k}"
+    for _ in range(args.warmup + args.steps):
+        call()
+    torch.cuda.synchronize()
+    err = phb.device_error()
+    print(json.dumps({"profile": what, "calls": args.warmup + args.steps, "device_error": err}))
+    if err:
+        raise SystemExit(1)
+
+
 # ----------------------------------------------------------------------------- main
 
 def main():
@@ -401,6 +441,10 @@ def main():
     ap.add_argument("--impl", default="phb", choices=["phb", "reference"])
     ap.add_argument("--headline-only", action="store_true", help="skip the extra rows")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=["decode", "decode-unfused", "prefill"],
+                    help="run only this path --steps times after --warmup calls (a small case for ncu) and print "
+                         "one status line instead of the bench line")
+    ap.add_argument("--layers", type=int, default=N_LAYERS, help="decode layers in --profile decode modes")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
@@ -417,6 +461,9 @@ def main():
     from quantized_decode_gguf_gb300 import build
     if rank == 0 or world == 1:
         build.build()
+    if args.profile:
+        run_profile(args)
+        return
     if world > 1:
         torch.distributed.barrier()
     import quantized_decode_gguf_gb300 as phb  # noqa: F401
@@ -445,7 +492,8 @@ def main():
 
     e2e_ms, h2d, d2h = bench_decode_e2e(ctx, max(20, args.steps // 2))
     kernels = bench_decode_kernels(ctx, seed)
-    dom = kernels["gate_up"]
+    unfused_ms = graph_time(lambda i: phb.decode_step("q8_0", ctx["table"], N_LAYERS, D_MODEL, N_Q, N_KV, HD, D_FF,
+                                                      ctx["x"], ctx["y"], ctx["ws"], fused=False), 1, iters=200)
     result = {
         "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
@@ -454,18 +502,24 @@ def main():
                                "SwiGLU 5632, all weights Q8_0 (1.15 GB per token)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (1.15 GB of weights streamed per step)",
-                   "graph": "one CUDA graph replay per step (96 kernels)"},
+                   "graph": "one CUDA graph replay per step: one cooperative decode_persistent_kernel launch"},
         "tok_per_s": tok_s,
         "pct_of_hbm_peak": 100.0 * gbs / world / peaks["hbm_gbs"],
-        "gpu_launches": 4 * N_LAYERS * args.steps,
+        "gpu_launches": args.steps,
         "clocks": clk.summary(),
         "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "tok_per_s": world / (e2e_ms * 1e-3),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "roofline": {"bound": "hbm", "kernel": "gemv_stream_kernel, fused Q8_0 gate/up 2x5632x2048 (SwiGLU), "
-                               "24 launches per CUDA graph over the 24 layers' weights",
-                     "achieved": dom["gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": dom["gbs"] / peaks["hbm_gbs"], "traffic": None,
-                     "peak_source": peaks["source"]},
+        # the step is one launch of the persistent kernel: its algorithmic bytes (all weights once plus the
+        # activation vectors) over the event-timed launch duration
+        "roofline": {"bound": "hbm", "kernel": "decode_persistent_kernel (Q8_0, 24 layers, one launch per step)",
+                     "achieved": step_bytes / (ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": step_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                     "traffic": DECODE_TRAFFIC_PER_LAUNCH if N_LAYERS == 24 else None,
+                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of a 4-layer launch, x6 "
+                                       "(profiles/decode_persistent_q8_0_24layer.md)",
+                     "bytes_per_launch": step_bytes, "peak_source": peaks["source"]},
+        "decode_launched": {"ms_per_step": unfused_ms, "gbs": step_bytes / (unfused_ms * 1e-3) / 1e9,
+                            "note": "phb_decode_step_unfused: 4 launches per layer in one CUDA graph"},
         "decode_kernels": kernels,
     }
     if not args.headline_only and rank == 0:
