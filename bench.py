@@ -414,6 +414,26 @@ def run_profile(args):
         call = lambda: phb.decode_step("q8_0", table, n_layers, D_MODEL, N_Q, N_KV, HD, D_FF, x, y, ws,  # noqa: E731
                                        fused=fused)
         what = f"{'fused' if fused else 'launched'} decode step, {n_layers} layers"
+    elif args.profile in ("moe1", "moe16"):
+        t_tokens = 1 if args.profile == "moe1" else 16
+        e, top_k, d_model, d_ff = 128, 8, 2048, 768
+        n_layers = args.layers if args.layers != N_LAYERS else 4
+        rb_in = row_bytes("q4_k", d_model)
+        mats = []
+        for layer in range(n_layers):
+            gu = synth.q4_k_blocks(seed, 2000 + layer, 2 * e * d_ff, d_model).reshape(2, e, d_ff, rb_in)
+            dn = synth.q4_k_blocks(seed, 3000 + layer, e * d_model, d_ff)
+            mats.append((torch.from_numpy(np.ascontiguousarray(gu[0])).cuda(),
+                         torch.from_numpy(np.ascontiguousarray(gu[1])).cuda(), torch.from_numpy(dn).cuda()))
+        x = torch.from_numpy(synth.normal_f32(seed, 1, (t_tokens, d_model))).cuda()
+        logits = [torch.from_numpy(synth.normal_f32(seed, 5000 + l, (t_tokens, e))).cuda() for l in range(n_layers)]
+        y = torch.empty_like(x)
+        ws = phb.workspace(phb.moe_workspace_size("q4_k", t_tokens, d_model, d_ff, e, top_k))
+
+        def call():
+            for l in range(n_layers):
+                phb.moe_ffn("q4_k", *mats[l], x, logits[l], d_model, d_ff, e, top_k, out=y, ws=ws)
+        what = f"MoE FFN Q4_K, {t_tokens} tokens, {n_layers} layers"
     else:
         n, k, m = 9728, 2560, 512
         w = torch.from_numpy(synth.blocks("q4_k", seed, 0, n, k)).cuda()
@@ -441,7 +461,7 @@ def main():
     ap.add_argument("--impl", default="phb", choices=["phb", "reference"])
     ap.add_argument("--headline-only", action="store_true", help="skip the extra rows")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["decode", "decode-unfused", "prefill"],
+    ap.add_argument("--profile", choices=["decode", "decode-unfused", "prefill", "moe1", "moe16"],
                     help="run only this path --steps times after --warmup calls (a small case for ncu) and print "
                          "one status line instead of the bench line")
     ap.add_argument("--layers", type=int, default=N_LAYERS, help="decode layers in --profile decode modes")

@@ -32,12 +32,22 @@ cudaError_t read_dev_err_moe(int* code) {
     return e;
 }
 
+#ifdef PHB_TRACE
+extern "C" int phb_trace_read_moe(void* dst, size_t bytes) {
+    if (bytes > sizeof(g_trace)) bytes = sizeof(g_trace);
+    return static_cast<int>(cudaMemcpyFromSymbol(dst, g_trace, bytes));
+}
+#endif
+
 namespace {
 
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 8;
 constexpr int kMaxTokens = 64;
-constexpr int kMoeGroup = 8;  // tokens per pass over a staged weight tile
+// Tokens per pass over a staged weight tile. Four keeps the staged
+// activations small enough for two CTAs per SM; an expert chosen by more
+// tokens streams its tile once per group of four.
+constexpr int kMoeGroup = 4;
 constexpr int kMoeCW = 8;     // consumer warps of the grouped kernels
 
 struct RouteOut {
@@ -50,57 +60,80 @@ struct RouteOut {
     int32_t* pair_list;  // [T*k]
 };
 
+// Order-preserving map of a finite float to an unsigned key (larger float,
+// larger key).
+__device__ __forceinline__ uint32_t float_key(float v) {
+    const uint32_t u = __float_as_uint(v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_float(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Routing. Warps take tokens; per token, K rounds of a warp-wide arg-max
+// (largest logit, then lowest expert index) over the logits held in
+// registers give the top_k in slot order, and lane 0 takes their softmax.
+// Then warp 0 sorts the (token, slot) pairs by expert with a stable
+// counting sort (match groups per 32 pairs, a warp scan over the experts)
+// and lists the active experts in ascending order.
 __global__ void __launch_bounds__(256) moe_route_kernel(const float* __restrict__ logits, int T, int E, int K,
-                                                        RouteOut o, int32_t* out_idx, float* out_p) {
+                                                        RouteOut o, int32_t* out_idx, float* out_p, int trace_id) {
+    (void)trace_id;
+    if (threadIdx.x == 0) PHB_TRACE_EV(trace_id, 0);
     pdl_launch_dependents();
     pdl_wait();
+    if (threadIdx.x == 0) PHB_TRACE_EV(trace_id, 1);
     __shared__ int32_t sidx[kMaxTokens * kMaxTopK];
+    __shared__ int32_t rank[kMaxTokens * kMaxTopK];
     __shared__ int32_t cnt[kMaxExperts];
     __shared__ int32_t off[kMaxExperts];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nwarps = blockDim.x >> 5;
+    for (int e = tid; e < kMaxExperts; e += blockDim.x) cnt[e] = 0;
     for (int t = warp; t < T; t += nwarps) {
-        float v[kMaxExperts / 32];
-        uint32_t taken = 0;
+        uint32_t key[kMaxExperts / 32];
 #pragma unroll
         for (int j = 0; j < kMaxExperts / 32; ++j) {
             const int e = lane + 32 * j;
-            v[j] = e < E ? logits[static_cast<int64_t>(t) * E + e] : -FLT_MAX;
+            key[j] = e < E ? float_key(logits[static_cast<int64_t>(t) * E + e]) : 0u;
         }
+        uint32_t taken = 0;
         float sel_v[kMaxTopK];
         int sel_e[kMaxTopK];
-        for (int r = 0; r < K; ++r) {
-            float bv = -FLT_MAX;
+#pragma unroll
+        for (int r = 0; r < kMaxTopK; ++r) {
+            if (r >= K) break;
+            // this lane's best untaken expert: largest key, then lowest index (ascending j)
+            uint32_t bk = 0;
             int be = 0x7FFFFFFF;
 #pragma unroll
             for (int j = 0; j < kMaxExperts / 32; ++j) {
                 const int e = lane + 32 * j;
-                if (e < E && !((taken >> j) & 1u) && (v[j] > bv || (v[j] == bv && e < be))) {
-                    bv = v[j];
+                if (e < E && !((taken >> j) & 1u) && (be == 0x7FFFFFFF || key[j] > bk)) {
+                    bk = key[j];
                     be = e;
                 }
             }
-#pragma unroll
-            for (int s = 16; s > 0; s >>= 1) {
-                const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, s);
-                const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, s);
-                if (ov > bv || (ov == bv && oe < be)) {
-                    bv = ov;
-                    be = oe;
-                }
-            }
-            if ((be & 31) == lane) taken |= 1u << (be >> 5);
-            sel_v[r] = bv;
-            sel_e[r] = be;
+            const uint32_t kmax = __reduce_max_sync(0xFFFFFFFFu, bk);
+            const uint32_t emin = __reduce_min_sync(0xFFFFFFFFu, (be != 0x7FFFFFFF && bk == kmax)
+                                                                     ? static_cast<uint32_t>(be) : 0xFFFFFFFFu);
+            if (static_cast<int>(emin & 31u) == lane) taken |= 1u << (emin >> 5);
+            sel_v[r] = key_float(kmax);
+            sel_e[r] = static_cast<int>(emin);
         }
         if (lane == 0) {
             float ex[kMaxTopK];
             float sum = 0.f;
-            for (int r = 0; r < K; ++r) {
+#pragma unroll
+            for (int r = 0; r < kMaxTopK; ++r) {
+                if (r >= K) break;
                 ex[r] = expf(sel_v[r] - sel_v[0]);
                 sum += ex[r];
             }
-            for (int r = 0; r < K; ++r) {
+#pragma unroll
+            for (int r = 0; r < kMaxTopK; ++r) {
+                if (r >= K) break;
                 const float pr = ex[r] / sum;
                 const int q = t * K + r;
                 sidx[q] = sel_e[r];
@@ -113,33 +146,60 @@ __global__ void __launch_bounds__(256) moe_route_kernel(const float* __restrict_
     }
     __syncthreads();
     const int pairs = T * K;
-    for (int e = tid; e < E; e += blockDim.x) {
-        int c = 0;
-        for (int q = 0; q < pairs; ++q) c += (sidx[q] == e);
-        cnt[e] = c;
-    }
-    __syncthreads();
-    if (tid == 0) {
-        int a = 0, acc = 0;
-        for (int e = 0; e < E; ++e) {
-            off[e] = acc;
-            if (cnt[e] > 0) {
-                o.act_expert[a] = e;
-                o.act_off[a] = acc;
-                o.act_cnt[a] = cnt[e];
-                ++a;
-                acc += cnt[e];
+    if (warp == 0) {
+        // stable rank of every pair within its expert, 32 pairs at a time
+        for (int q0 = 0; q0 < pairs; q0 += 32) {
+            const int q = q0 + lane;
+            const bool valid = q < pairs;
+            const int e = valid ? sidx[q] : -1 - lane;  // invalid lanes match nobody
+            const unsigned grp = __match_any_sync(0xFFFFFFFFu, e);
+            const int base = valid ? cnt[e] : 0;
+            __syncwarp();
+            if (valid) {
+                rank[q] = base + __popc(grp & ((1u << lane) - 1u));
+                if ((__ffs(grp) - 1) == lane) cnt[e] = base + __popc(grp);
+            }
+            __syncwarp();
+        }
+        // exclusive scan over experts (8 consecutive experts per lane) and the active list
+        constexpr int kPer = kMaxExperts / 32;
+        int c[kPer], lc = 0, la = 0;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const int e = kPer * lane + i;
+            c[i] = e < E ? cnt[e] : 0;
+            lc += c[i];
+            la += c[i] > 0;
+        }
+        int sc = lc, sa = la;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int vc = __shfl_up_sync(0xFFFFFFFFu, sc, d), va = __shfl_up_sync(0xFFFFFFFFu, sa, d);
+            if (lane >= d) {
+                sc += vc;
+                sa += va;
             }
         }
-        *o.n_active = a;
+        int acc = sc - lc, a = sa - la;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const int e = kPer * lane + i;
+            if (e < E) {
+                off[e] = acc;
+                if (c[i] > 0) {
+                    o.act_expert[a] = e;
+                    o.act_off[a] = acc;
+                    o.act_cnt[a] = c[i];
+                    ++a;
+                }
+                acc += c[i];
+            }
+        }
+        if (lane == 31) *o.n_active = sa;
     }
     __syncthreads();
-    for (int e = tid; e < E; e += blockDim.x) {
-        if (cnt[e] == 0) continue;
-        int w = off[e];
-        for (int q = 0; q < pairs; ++q)
-            if (sidx[q] == e) o.pair_list[w++] = q;
-    }
+    for (int q = tid; q < pairs; q += blockDim.x) o.pair_list[off[sidx[q]] + rank[q]] = q;
+    if (threadIdx.x == 0) PHB_TRACE_EV(trace_id, 3);
 }
 
 struct MoeParams {
@@ -160,6 +220,7 @@ struct MoeParams {
     const uint8_t* pf;        // per-expert matrix to prefetch into L2 (the down matrix), or null
     int64_t pf_stride;        // its bytes per expert
     uint32_t xs_off, xsum_off, part_off, acc_off, bar_off;
+    int trace_id;
 };
 
 template <int QT, int NMAT, int MAXB>
@@ -182,6 +243,7 @@ __device__ __forceinline__ bool moe_group(const MoeParams& p, const Tile& t, int
         for (int i = tid; i < NMAT * t.rows_here * kAccStride; i += KCfg<QT, kMoeCW>::consumers) row_acc[i] = 0.f;
     consumer_sync<KCfg<QT, kMoeCW>::consumers>();
     stage_x<kMoeCW, MAXB, kXRowList>(p.x, p.ldx, 0, kseg, nb, xs, xsum, xfac, red, 1, 1, 0, rowidx);
+    if (tid == 0) PHB_TRACE_EV(p.trace_id, 2);
     const int* pairs = p.r.pair_list + first_pair_idx;
     auto epi = [&](int r, int b, float a0, float a1) {
         const float out = NMAT == 2 ? silu_mul(a0, a1) : a0;
@@ -195,13 +257,15 @@ __device__ __forceinline__ bool moe_group(const MoeParams& p, const Tile& t, int
 }
 
 template <int QT, int NMAT>
-__global__ void __launch_bounds__(KCfg<QT, kMoeCW>::threads, 1) moe_stream_kernel(const __grid_constant__ MoeParams p) {
+__global__ void __launch_bounds__(KCfg<QT, kMoeCW>::threads, 2) moe_stream_kernel(const __grid_constant__ MoeParams p) {
     using C = KCfg<QT, kMoeCW>;
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
     uint64_t* empty = full + C::ns;
+    if (threadIdx.x == 0) PHB_TRACE_EV(p.trace_id, 0);
     pdl_launch_dependents();
     pdl_wait();  // routing results (and, for the down pass, h) come from the previous kernels
+    if (threadIdx.x == 0) PHB_TRACE_EV(p.trace_id, 1);
     const int slot = blockIdx.y;
     if (slot >= *p.r.n_active) return;
     const int e = p.r.act_expert[slot];
@@ -249,24 +313,29 @@ __global__ void __launch_bounds__(KCfg<QT, kMoeCW>::threads, 1) moe_stream_kerne
             ok = moe_group<QT, NMAT, 1>(p, t, row0, fp, nb, smem, full, empty, s);
         else if (nb == 2)
             ok = moe_group<QT, NMAT, 2>(p, t, row0, fp, nb, smem, full, empty, s);
-        else if (nb <= 4)
-            ok = moe_group<QT, NMAT, 4>(p, t, row0, fp, nb, smem, full, empty, s);
         else
-            ok = moe_group<QT, NMAT, 8>(p, t, row0, fp, nb, smem, full, empty, s);
+            ok = moe_group<QT, NMAT, 4>(p, t, row0, fp, nb, smem, full, empty, s);
         if (!ok) return;
     }
+    consumer_sync<C::consumers>();
+    if (tid == 0) PHB_TRACE_EV(p.trace_id, 3);
 }
 
 __global__ void __launch_bounds__(256) moe_combine_kernel(const float* __restrict__ yp, const float* __restrict__ p,
-                                                          float* __restrict__ y, int T, int K, int64_t D) {
+                                                          float* __restrict__ y, int T, int K, int64_t D,
+                                                          int trace_id) {
+    (void)trace_id;
+    if (threadIdx.x == 0) PHB_TRACE_EV(trace_id, 0);
     pdl_launch_dependents();
     pdl_wait();
+    if (threadIdx.x == 0) PHB_TRACE_EV(trace_id, 1);
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i >= static_cast<int64_t>(T) * D) return;
     const int64_t t = i / D, d = i - t * D;
     float acc = 0.f;
     for (int s = 0; s < K; ++s) acc = fmaf(p[t * K + s], yp[(t * K + s) * D + d], acc);
     y[i] = acc;
+    if (threadIdx.x == 0) PHB_TRACE_EV(trace_id, 3);
 }
 
 struct MoeWs {
@@ -310,15 +379,23 @@ cudaError_t launch_moe_stream(const MoeParams& p, dim3 grid, size_t smem, cudaSt
     return launch_kernel(kern, grid, dim3(KCfg<QT, kMoeCW>::threads), smem, s, true, p);
 }
 
-// Rows per CTA and shared-memory layout of one grouped pass.
-bool plan_moe(int qt, int nmat, int64_t n, int64_t k, int cpe, MoeParams* p, unsigned* gx, size_t* smem) {
+// Rows per CTA and shared-memory layout of one grouped pass. `maxb` is the
+// largest token group (at most the token count). A CTA gets at most about 8
+// stages of weights per token group, and few enough rows that its row sums fit
+// the tile partials (the fold mode synchronises the CTA at every stage).
+bool plan_moe(int qt, int nmat, int64_t n, int64_t k, int cpe, int maxb, MoeParams* p, unsigned* gx,
+              size_t* smem) {
     const int units_row = static_cast<int>(k / kUnitWeights);
     int rows_per_cta = static_cast<int>(cdiv(n, cpe));
+    rows_per_cta = std::min(rows_per_cta, std::max(1, 8 * KCfg<0, kMoeCW>::stage_units / (nmat * units_row)));
     SmemLayout lay{};
     for (;;) {
-        lay = stream_smem_layout(qt, kMoeCW, nmat, kMoeGroup, rows_per_cta, units_row);
-        if (lay.total <= kSmemOptin) break;
-        if (rows_per_cta == 1) return false;
+        lay = stream_smem_layout(qt, kMoeCW, nmat, maxb, rows_per_cta, units_row);
+        if (lay.total <= kSmemOptin && lay.sum_mode != kSumFold) break;
+        if (rows_per_cta == 1) {
+            if (lay.total <= kSmemOptin) break;
+            return false;
+        }
         rows_per_cta = (rows_per_cta + 1) / 2;
     }
     p->units_row = units_row;
@@ -343,10 +420,16 @@ size_t moe_ws_bytes(const MoeReq& q) { return moe_ws_layout(q, nullptr).bytes; }
 
 cudaError_t moe_run(const MoeReq& q, cudaStream_t s) {
     const MoeWs w = moe_ws_layout(q, q.ws);
+#ifdef PHB_TRACE
+    static int trace_call = 0;  // debug builds: 4 trace slots per call, 32 calls
+    const int tb = 4 * (trace_call++ % 32);
+#else
+    const int tb = -1000;
+#endif
     const int pairs = static_cast<int>(q.t * q.top_k);
     const int slots = std::min(q.e, pairs);
     cudaError_t e = launch_kernel(moe_route_kernel, dim3(1), dim3(256), 0, s, true, q.logits, static_cast<int>(q.t),
-                                  q.e, q.top_k, w.r, q.out_idx, q.out_p);
+                                  q.e, q.top_k, w.r, q.out_idx, q.out_p, tb);
     if (e != cudaSuccess) return e;
     // CTAs per expert: enough to cover the GPU twice for the expected number
     // of distinct experts, E * (1 - (1 - k/E)^T).
@@ -357,7 +440,9 @@ cudaError_t moe_run(const MoeReq& q, cudaStream_t s) {
     MoeParams pg{};
     unsigned gx = 0;
     size_t smem = 0;
-    if (!plan_moe(q.qt, 2, q.d_ff, q.d_model, cpe, &pg, &gx, &smem)) return cudaErrorInvalidConfiguration;
+    // tokens per expert never exceed the token count: size the staged activations for that
+    const int maxb = maxb_for(static_cast<int>(std::min<int64_t>(kMoeGroup, q.t)));
+    if (!plan_moe(q.qt, 2, q.d_ff, q.d_model, cpe, maxb, &pg, &gx, &smem)) return cudaErrorInvalidConfiguration;
     pg.w[0] = static_cast<const uint8_t*>(q.wg);
     pg.w[1] = static_cast<const uint8_t*>(q.wu);
     pg.x = q.x;
@@ -368,13 +453,14 @@ cudaError_t moe_run(const MoeReq& q, cudaStream_t s) {
     pg.ldy = q.d_ff;
     pg.r = w.r;
     pg.pf = static_cast<const uint8_t*>(q.wd);
+    pg.trace_id = tb + 1;
     pg.pf_stride = q.d_model * static_cast<int64_t>(q.qt == 0 ? q.d_ff / 32 * 34 : q.d_ff / 256 * 144);
     e = q.qt == 0 ? launch_moe_stream<0, 2>(pg, dim3(gx, slots), smem, s)
                   : launch_moe_stream<1, 2>(pg, dim3(gx, slots), smem, s);
     if (e != cudaSuccess) return e;
 
     MoeParams pd{};
-    if (!plan_moe(q.qt, 1, q.d_model, q.d_ff, cpe, &pd, &gx, &smem)) return cudaErrorInvalidConfiguration;
+    if (!plan_moe(q.qt, 1, q.d_model, q.d_ff, cpe, maxb, &pd, &gx, &smem)) return cudaErrorInvalidConfiguration;
     pd.w[0] = pd.w[1] = static_cast<const uint8_t*>(q.wd);
     pd.x = w.h;
     pd.ldx = q.d_ff;
@@ -383,6 +469,7 @@ cudaError_t moe_run(const MoeReq& q, cudaStream_t s) {
     pd.y = w.yp;
     pd.ldy = q.d_model;
     pd.r = w.r;
+    pd.trace_id = tb + 2;
     e = q.qt == 0 ? launch_moe_stream<0, 1>(pd, dim3(gx, slots), smem, s)
                   : launch_moe_stream<1, 1>(pd, dim3(gx, slots), smem, s);
     if (e != cudaSuccess) return e;
@@ -390,7 +477,7 @@ cudaError_t moe_run(const MoeReq& q, cudaStream_t s) {
     const int64_t total = q.t * q.d_model;
     return launch_kernel(moe_combine_kernel, dim3(static_cast<unsigned>(cdiv(total, 256))), dim3(256), 0, s, true,
                          static_cast<const float*>(w.yp), static_cast<const float*>(w.r.p), q.y,
-                         static_cast<int>(q.t), q.top_k, q.d_model);
+                         static_cast<int>(q.t), q.top_k, q.d_model, tb + 3);
 }
 
 }  // namespace phb
