@@ -414,6 +414,15 @@ def run_profile(args):
         call = lambda: phb.decode_step("q8_0", table, n_layers, D_MODEL, N_Q, N_KV, HD, D_FF, x, y, ws,  # noqa: E731
                                        fused=fused)
         what = f"{'fused' if fused else 'launched'} decode step, {n_layers} layers"
+    elif args.profile == "gemv":
+        qt, n, k, b = args.gemv.split(",")
+        n, k, b = int(n), int(k), int(b)
+        w = torch.from_numpy(synth.blocks(qt, seed, 0, n, k)).cuda()
+        x = torch.from_numpy(synth.normal_f32(seed, 1, (b, k))).cuda()
+        y = torch.empty((b, n), device="cuda")
+        ws = phb.workspace(phb.gemv_workspace_size(qt, n, k, b))
+        call = lambda: phb.gemv(qt, w, x, n, k, out=y, ws=ws)  # noqa: E731
+        what = f"GEMV {qt} {n}x{k} batch {b}"
     elif args.profile in ("moe1", "moe16"):
         t_tokens = 1 if args.profile == "moe1" else 16
         e, top_k, d_model, d_ff = 128, 8, 2048, 768
@@ -461,10 +470,11 @@ def main():
     ap.add_argument("--impl", default="phb", choices=["phb", "reference"])
     ap.add_argument("--headline-only", action="store_true", help="skip the extra rows")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["decode", "decode-unfused", "prefill", "moe1", "moe16"],
+    ap.add_argument("--profile", choices=["decode", "decode-unfused", "prefill", "moe1", "moe16", "gemv"],
                     help="run only this path --steps times after --warmup calls (a small case for ncu) and print "
                          "one status line instead of the bench line")
     ap.add_argument("--layers", type=int, default=N_LAYERS, help="decode layers in --profile decode modes")
+    ap.add_argument("--gemv", default="q4_k,9728,2560,4", help="--profile gemv case: qtype,n,k,batch")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -107,8 +107,15 @@ cudaError_t swiglu_run(const float* g, const float* u, float* h, int64_t count, 
                          count);
 }
 
+// Batched plain GEMVs take the row-resident kernel (gemv_rows.cu). At batch 1
+// the streaming kernel is as fast or faster (no split-K pass for short K).
+static bool use_rows_kernel(const GemvReq& q) {
+    return q.batch >= 2 && q.nmat == 1 && q.xmode == kXPlain && q.epi == kEpiStore && q.k % kUnitWeights == 0;
+}
+
 size_t gemv_ws_floats(const GemvReq& q) {
     if (q.k % kUnitWeights != 0) return 0;
+    if (use_rows_kernel(q)) return gemv_rows_ws_floats(q.qt, q.n, q.k, q.batch);
     const int ks = plan_ksplit(q);
     return ks > 1 ? static_cast<size_t>(ks) * q.batch * q.n : 0;
 }
@@ -121,6 +128,22 @@ static cudaError_t dispatch_maxb(const GemvPlan& pl, int maxb, cudaStream_t s, b
         case 4: return run_stream<QT, 4, NMAT, kXPlain, EPI>(pl, s, pdl);
         default: return run_stream<QT, 8, NMAT, kXPlain, EPI>(pl, s, pdl);
     }
+}
+
+template <int QT, int NMAT, int EPI>
+static int ctas_per_sm_maxb(int maxb) {
+    switch (maxb) {
+        case 1: return stream_ctas_per_sm<QT, 1, NMAT, kXPlain, EPI>();
+        case 2: return stream_ctas_per_sm<QT, 2, NMAT, kXPlain, EPI>();
+        case 4: return stream_ctas_per_sm<QT, 4, NMAT, kXPlain, EPI>();
+        default: return stream_ctas_per_sm<QT, 8, NMAT, kXPlain, EPI>();
+    }
+}
+
+static int ctas_per_sm_for(int qt, int maxb, int nmat) {
+    if (nmat == 2)
+        return qt == 0 ? ctas_per_sm_maxb<0, 2, kEpiSwiGLU>(maxb) : ctas_per_sm_maxb<1, 2, kEpiSwiGLU>(maxb);
+    return qt == 0 ? ctas_per_sm_maxb<0, 1, kEpiStore>(maxb) : ctas_per_sm_maxb<1, 1, kEpiStore>(maxb);
 }
 
 cudaError_t gemv_run(const GemvReq& q, cudaStream_t s) {
@@ -141,8 +164,16 @@ cudaError_t gemv_run(const GemvReq& q, cudaStream_t s) {
         }
     }
     if (q.xmode != kXPlain) return cudaErrorInvalidValue;
+    if (use_rows_kernel(q)) {
+        int ks = 1;
+        cudaError_t e = gemv_rows_run(q, s, &ks);
+        if (e != cudaSuccess || ks == 1) return e;
+        const int64_t total = static_cast<int64_t>(q.batch) * q.n;
+        return launch_kernel(splitk_reduce_kernel, dim3(static_cast<unsigned>(cdiv(total, 256))), dim3(256), 0, s,
+                             q.pdl, static_cast<const float*>(q.ws), q.y, q.n, q.batch, ks, q.ldy);
+    }
     GemvPlan pl;
-    if (!plan_stream(q, &pl)) return cudaErrorInvalidConfiguration;
+    if (!plan_stream(q, &pl, ctas_per_sm_for(q.qt, maxb, q.nmat))) return cudaErrorInvalidConfiguration;
     const int ks = static_cast<int>(pl.grid.y);
     if (ks > 1 && (q.ws == nullptr || q.ws_floats < static_cast<size_t>(ks) * q.batch * q.n))
         return cudaErrorInvalidValue;

@@ -455,7 +455,10 @@ struct GemvParams {
 };
 
 template <int QT, int CW, int MAXB, int NMAT, int XMODE, int EPI>
-__global__ void __launch_bounds__(KCfg<QT, CW>::threads, 1) gemv_stream_kernel(const __grid_constant__ GemvParams p) {
+// Batch 1 and 2: registers capped so that two CTAs share an SM; larger
+// batches hold more accumulators and run one wider CTA per SM.
+__global__ void __launch_bounds__(KCfg<QT, CW>::threads, MAXB <= 2 ? 2 : 1)
+    gemv_stream_kernel(const __grid_constant__ GemvParams p) {
     using C = KCfg<QT, CW>;
     extern __shared__ __align__(1024) uint8_t smem[];
     float* xs = reinterpret_cast<float*>(smem + p.xs_off);

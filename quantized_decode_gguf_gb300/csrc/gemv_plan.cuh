@@ -27,10 +27,12 @@ inline int plan_ksplit(const GemvReq& q) {
     return static_cast<int>(cdiv(units_row, seg));
 }
 
-// Eight consumer warps: a CTA takes about half an SM, so the next kernel in
-// a programmatic-dependent chain can be resident and stream its weights
-// while this one finishes.
-constexpr int cw_for(int) { return 8; }
+// Consumer warps per CTA. Batch 1 and 2: eight, a CTA takes about half an
+// SM, so the next kernel in a programmatic-dependent chain can be resident
+// and stream its weights while this one finishes. Batch 3..8 needs more
+// registers per thread (128 to 168) and fills one SM with as many warps as
+// the register file then holds: 12 + 1 at <= 128, 11 + 1 at <= 168.
+constexpr int cw_for(int maxb) { return maxb <= 2 ? 8 : maxb <= 4 ? 12 : 11; }
 
 // Dynamic shared memory of a streaming-GEMV CTA:
 //   stages | xs [maxb][xpad_len(kseg)] | xsum [maxb][kseg/32] |
@@ -87,7 +89,7 @@ inline SmemLayout stream_smem_layout(int qt, int cw, int nmat, int maxb, int row
 
 // Fill a launch plan (one CTA per SM per K split). Returns false if no
 // layout fits shared memory.
-inline bool plan_stream(const GemvReq& q, GemvPlan* pl) {
+inline bool plan_stream(const GemvReq& q, GemvPlan* pl, int ctas_per_sm = kCtasPerSm) {
     const int units_row = static_cast<int>(q.k / kUnitWeights);
     const int ksplit0 = plan_ksplit(q);
     const int units_seg = static_cast<int>(cdiv(units_row, ksplit0));
@@ -95,7 +97,7 @@ inline bool plan_stream(const GemvReq& q, GemvPlan* pl) {
     const int maxb = maxb_for(q.batch);
     const int cw = cw_for(maxb);
     const int sms = device_sm_count();
-    const int64_t target = std::max<int64_t>(1, cdiv(static_cast<int64_t>(sms) * kCtasPerSm, ksplit));
+    const int64_t target = std::max<int64_t>(1, cdiv(static_cast<int64_t>(sms) * ctas_per_sm, ksplit));
     int64_t nrow_ctas = std::min<int64_t>(q.n, target);
     int rows_per_cta = static_cast<int>(cdiv(q.n, nrow_ctas));
     SmemLayout lay{};
@@ -141,6 +143,22 @@ inline bool plan_stream(const GemvReq& q, GemvPlan* pl) {
     pl->smem = lay.total;
     pl->cw = cw;
     return true;
+}
+
+// CTAs of one streaming-GEMV instantiation that fit an SM (its registers
+// decide), at most kCtasPerSm; queried once per instantiation.
+template <int QT, int MAXB, int NMAT, int XMODE, int EPI>
+inline int stream_ctas_per_sm() {
+    static int cached = 0;
+    if (cached == 0) {
+        constexpr int CW = cw_for(MAXB);
+        constexpr auto kern = gemv_stream_kernel<QT, CW, MAXB, NMAT, XMODE, EPI>;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, KCfg<QT, CW>::threads, 0) != cudaSuccess || n < 1)
+            n = 1;
+        cached = std::min(n, kCtasPerSm);
+    }
+    return cached;
 }
 
 template <int QT, int MAXB, int NMAT, int XMODE, int EPI>

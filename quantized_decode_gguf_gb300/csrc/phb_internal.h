@@ -146,5 +146,12 @@ cudaError_t read_dev_err_decode(int* code);
 cudaError_t read_dev_err_moe(int* code);
 cudaError_t read_dev_err_prefill(int* code);
 cudaError_t read_dev_err_decode_persistent(int* code);
+cudaError_t read_dev_err_gemv_rows(int* code);
+
+// Row-resident batched GEMV (gemv_rows.cu): plain store, batch 2..8,
+// K % 256 == 0. ksplit_out receives the K splits (> 1: partials in q.ws
+// still need splitk reduction).
+size_t gemv_rows_ws_floats(int qt, int64_t n, int64_t k, int batch);
+cudaError_t gemv_rows_run(const GemvReq& q, cudaStream_t s, int* ksplit_out);
 
 }  // namespace phb
