@@ -4,18 +4,23 @@
 //    (ties to the lower expert index) and their softmax; then a counting sort
 //    of the (token, slot) pairs by expert, ascending pair id within an
 //    expert, giving the active-expert list.
-// 2. moe_stream_kernel<NMAT=2>: grid (CTAs per expert, expert slot). Each CTA
-//    streams a row range of its expert's gate and up matrices once and
-//    applies it to every token routed to that expert (groups of up to 8),
-//    writing h[pair] = silu(gate.x) * (up.x).
-// 3. moe_stream_kernel<NMAT=1>: the same over the down matrices, x = h[pair],
-//    writing y_pair[pair].
+// 2. moe_rows_kernel<NMAT=2>: grid (row tiles of 64, expert slot). Each CTA
+//    streams 64 rows of its expert's gate and up matrices (one 3-D TMA copy
+//    per matrix and 256-weight unit) once per group of up to four tokens
+//    routed to that expert, keeps every row's per-token sums in registers
+//    and writes h[pair] = silu(gate.x) * (up.x).
+// 3. moe_rows_kernel<NMAT=1>: the same over 128 rows of the down matrices,
+//    x = h[pair], writing y_pair[pair].
 // 4. moe_combine_kernel: y[t] = sum over slots (ascending) of p[t][slot] *
 //    y_pair[t*top_k + slot].
 // All orders are fixed, so repeated calls give identical bits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <algorithm>
 #include <cfloat>
 #include <cmath>
+#include <mutex>
 
 #include "gemv_plan.cuh"
 #include "phb_internal.h"
@@ -48,7 +53,7 @@ constexpr int kMaxTokens = 64;
 // activations small enough for two CTAs per SM; an expert chosen by more
 // tokens streams its tile once per group of four.
 constexpr int kMoeGroup = 4;
-constexpr int kMoeCW = 8;     // consumer warps of the grouped kernels
+
 
 struct RouteOut {
     int32_t* idx;        // [T][k]
@@ -202,125 +207,6 @@ __global__ void __launch_bounds__(256) moe_route_kernel(const float* __restrict_
     if (threadIdx.x == 0) PHB_TRACE_EV(trace_id, 3);
 }
 
-struct MoeParams {
-    const uint8_t* w[2];      // expert 0 of each matrix
-    int64_t expert_stride;    // bytes per expert matrix
-    int64_t row_bytes;
-    int64_t n;                // rows per expert matrix
-    int units_row;
-    int rows_per_cta;
-    const float* x;           // gate/up: X [T][K]; down: h [pairs][K]
-    int64_t ldx;
-    int x_by_pair;            // 0: x row = pair / top_k; 1: x row = pair
-    int top_k;
-    float* y;                 // [pairs][n]
-    int64_t ldy;
-    RouteOut r;
-    int sum_mode;
-    const uint8_t* pf;        // per-expert matrix to prefetch into L2 (the down matrix), or null
-    int64_t pf_stride;        // its bytes per expert
-    uint32_t xs_off, xsum_off, part_off, acc_off, bar_off;
-    int trace_id;
-};
-
-template <int QT, int NMAT, int MAXB>
-__device__ __forceinline__ bool moe_group(const MoeParams& p, const Tile& t, int row0, int first_pair_idx, int nb,
-                                          uint8_t* smem, uint64_t* full, uint64_t* empty, int& s) {
-    float* xs = reinterpret_cast<float*>(smem + p.xs_off);
-    float* xsum = reinterpret_cast<float*>(smem + p.xsum_off);
-    float* part = reinterpret_cast<float*>(smem + p.part_off);
-    float* row_acc = reinterpret_cast<float*>(smem + p.acc_off);
-    float* xfac = reinterpret_cast<float*>(full + 2 * KCfg<QT, kMoeCW>::ns);
-    float* red = xfac + kAccStride;
-    int* rowidx = reinterpret_cast<int*>(red + (2 * kMaxConsumerWarps + 3) * kAccStride);
-    const int tid = threadIdx.x;
-    const int kseg = t.useg * kUnitWeights;
-    if (tid < nb) {
-        const int pair = p.r.pair_list[first_pair_idx + tid];
-        rowidx[tid] = p.x_by_pair ? pair : pair / p.top_k;
-    }
-    if (p.sum_mode == kSumFold)
-        for (int i = tid; i < NMAT * t.rows_here * kAccStride; i += KCfg<QT, kMoeCW>::consumers) row_acc[i] = 0.f;
-    consumer_sync<KCfg<QT, kMoeCW>::consumers>();
-    stage_x<kMoeCW, MAXB, kXRowList>(p.x, p.ldx, 0, kseg, nb, xs, xsum, xfac, red, 1, 1, 0, rowidx);
-    if (tid == 0) PHB_TRACE_EV(p.trace_id, 2);
-    const int* pairs = p.r.pair_list + first_pair_idx;
-    auto epi = [&](int r, int b, float a0, float a1) {
-        const float out = NMAT == 2 ? silu_mul(a0, a1) : a0;
-        p.y[static_cast<int64_t>(pairs[b]) * p.ldy + row0 + r] = out;
-    };
-    if (!consume_tile<QT, kMoeCW, MAXB, NMAT>(t, p.sum_mode, smem, full, empty, s, xs, xpad_len(kseg), xsum,
-                                              kseg / 32, xfac, nb, part, row_acc, epi))
-        return false;
-    consumer_sync<KCfg<QT, kMoeCW>::consumers>();  // the next group overwrites xs, xsum and row_acc
-    return true;
-}
-
-template <int QT, int NMAT>
-__global__ void __launch_bounds__(KCfg<QT, kMoeCW>::threads, 2) moe_stream_kernel(const __grid_constant__ MoeParams p) {
-    using C = KCfg<QT, kMoeCW>;
-    extern __shared__ __align__(1024) uint8_t smem[];
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
-    uint64_t* empty = full + C::ns;
-    if (threadIdx.x == 0) PHB_TRACE_EV(p.trace_id, 0);
-    pdl_launch_dependents();
-    pdl_wait();  // routing results (and, for the down pass, h) come from the previous kernels
-    if (threadIdx.x == 0) PHB_TRACE_EV(p.trace_id, 1);
-    const int slot = blockIdx.y;
-    if (slot >= *p.r.n_active) return;
-    const int e = p.r.act_expert[slot];
-    const int first = p.r.act_off[slot];
-    const int cnt = p.r.act_cnt[slot];
-    const int row0 = blockIdx.x * p.rows_per_cta;
-    Tile t;
-    t.rows_here = static_cast<int>(min(static_cast<int64_t>(p.rows_per_cta), p.n - row0));
-    if (t.rows_here <= 0) return;
-    t.useg = p.units_row;
-    t.row_bytes = p.row_bytes;
-    t.contiguous = true;
-    t.w[0] = p.w[0] + e * p.expert_stride + static_cast<int64_t>(row0) * p.row_bytes;
-    t.w[1] = p.w[NMAT - 1] + e * p.expert_stride + static_cast<int64_t>(row0) * p.row_bytes;
-    const int tid = threadIdx.x;
-    if (tid == 0) {
-        for (int s = 0; s < C::ns; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kMoeCW);
-        }
-        fence_barrier_init();
-    }
-    __syncthreads();
-    const int ngroups = (cnt + kMoeGroup - 1) / kMoeGroup;
-    if (tid >= C::consumers) {
-        if (tid == C::consumers) {
-            const uint64_t pol = policy_evict_first();
-            int s = 0;
-            for (int gi = 0; gi < ngroups; ++gi)
-                if (!produce_tile<QT, kMoeCW>(t, NMAT, smem, full, empty, s, pol)) break;
-        } else if (tid == C::consumers + 1 && p.pf != nullptr && blockIdx.x == 0) {
-            // the expert's down matrix, needed by the next kernel
-            const uint8_t* base = p.pf + e * p.pf_stride;
-            for (int64_t off = 0; off < p.pf_stride; off += 32768)
-                prefetch_l2(base + off, static_cast<uint32_t>(p.pf_stride - off < 32768 ? p.pf_stride - off : 32768));
-        }
-        return;
-    }
-    int s = 0;
-    for (int gi = 0; gi < ngroups; ++gi) {
-        const int nb = min(kMoeGroup, cnt - gi * kMoeGroup);
-        const int fp = first + gi * kMoeGroup;
-        bool ok;
-        if (nb == 1)
-            ok = moe_group<QT, NMAT, 1>(p, t, row0, fp, nb, smem, full, empty, s);
-        else if (nb == 2)
-            ok = moe_group<QT, NMAT, 2>(p, t, row0, fp, nb, smem, full, empty, s);
-        else
-            ok = moe_group<QT, NMAT, 4>(p, t, row0, fp, nb, smem, full, empty, s);
-        if (!ok) return;
-    }
-    consumer_sync<C::consumers>();
-    if (tid == 0) PHB_TRACE_EV(p.trace_id, 3);
-}
-
 __global__ void __launch_bounds__(256) moe_combine_kernel(const float* __restrict__ yp, const float* __restrict__ p,
                                                           float* __restrict__ y, int T, int K, int64_t D,
                                                           int trace_id) {
@@ -336,6 +222,246 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const float* __restric
     for (int s = 0; s < K; ++s) acc = fmaf(p[t * K + s], yp[(t * K + s) * D + d], acc);
     y[i] = acc;
     if (threadIdx.x == 0) PHB_TRACE_EV(trace_id, 3);
+}
+
+// ---------------------------------------------------------------- row-resident grouped kernel
+// The expert-grouped pass with the row-resident mapping of gemv_rows.cu: a
+// CTA owns 128 rows of one active expert (for gate/up: 64 gate rows and the
+// same 64 up rows), each stage is one 256-weight unit of those rows brought
+// by one 3-D TMA copy per matrix ([expert][rows][row bytes]), thread t keeps
+// row t % 128's sums for up to four tokens in registers over half unit
+// t / 128, and the activations are shared-memory broadcasts.
+constexpr int kMrRows = 128;
+constexpr int kMrCW = 8;
+constexpr int kMrNC = 32 * kMrCW;
+constexpr int kMrThreads = kMrNC + 32;
+
+template <int QT>
+struct MrCfg {
+    static constexpr int ub = Fmt<QT>::unit_bytes;
+    static constexpr int stage_bytes = kMrRows * ub;
+    static constexpr int ns = QT == 0 ? 3 : 6;
+};
+
+struct MoeRowsParams {
+    const float* x;        // gate/up: X [T][K]; down: h [pairs][K]
+    int64_t ldx;
+    int x_by_pair;         // 0: x row = pair / top_k; 1: x row = pair
+    int top_k;
+    float* y;              // [pairs][n]
+    int64_t ldy;
+    RouteOut r;
+    int64_t n;             // rows per expert matrix
+    int units_row;
+    int row_tile;          // rows of each matrix per CTA: 64 (gate/up) or 128 (down)
+    uint32_t xs_off, xsum_off, comb_off, bar_off;
+    int trace_id;
+};
+
+__device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* map, int x, int y, int z,
+                                                 uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+        "%3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+// One token group (nb <= MAXB tokens) over the CTA's rows: stage the tokens'
+// activations, stream every unit, write silu(gate) * up (NMAT 2) or the row
+// sums (NMAT 1) for each token.
+template <int QT, int NMAT, int MAXB>
+__device__ __forceinline__ bool moe_rows_group(const MoeRowsParams& p, int64_t row0, int first, int nb, uint8_t* smem,
+                                               uint64_t* full, uint64_t* empty, int& s) {
+    using R = MrCfg<QT>;
+    float* xs = reinterpret_cast<float*>(smem + p.xs_off);
+    float* xsum = reinterpret_cast<float*>(smem + p.xsum_off);
+    float* comb = reinterpret_cast<float*>(smem + p.comb_off);  // [2][MAXB][128]
+    float* xfac = reinterpret_cast<float*>(full + 2 * R::ns);
+    float* red = xfac + kAccStride;
+    int* rowidx = reinterpret_cast<int*>(red + (2 * kMaxConsumerWarps + 3) * kAccStride);
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int kseg = p.units_row * kUnitWeights;
+    if (tid < nb) {
+        const int pair = p.r.pair_list[first + tid];
+        rowidx[tid] = p.x_by_pair ? pair : pair / p.top_k;
+    }
+    consumer_sync<kMrNC>();
+    stage_x<kMrCW, MAXB, kXRowList>(p.x, p.ldx, 0, kseg, nb, xs, xsum, xfac, red, 1, 1, 0, rowidx);
+    const int row = tid & (kMrRows - 1);
+    const int h = tid >> 7;
+    const int xstride = xpad_len(kseg), sstride = kseg / 32;
+    float acc[MAXB];
+#pragma unroll
+    for (int b = 0; b < MAXB; ++b) acc[b] = 0.f;
+    for (int u = 0; u < p.units_row; ++u, ++s) {
+        const int slot = s % R::ns;
+        int good = 1;
+        if (lane == 0) good = mbar_wait(&full[slot], (s / R::ns) & 1, &g_dev_err) ? 1 : 0;
+        good = __shfl_sync(0xFFFFFFFFu, good, 0);
+        __syncwarp();
+        if (!good) return false;
+        const uint8_t* ub = smem + slot * R::stage_bytes + row * R::ub;
+        const int hu = 2 * u + h;
+        if constexpr (QT == 0)
+            dot_q8_0_half<MAXB>(ub + 136 * h, xs + hu * (kXPadEvery + kXPad), xstride, xsum + hu * 4, sstride, xfac,
+                                acc);
+        else
+            dot_q4_k_half<MAXB>(ub, h, xs + hu * (kXPadEvery + kXPad), xstride, xsum + hu * 4, sstride, xfac, acc);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+    }
+    // halves of a row meet, then (NMAT 2) gate row r and up row r
+    if (h == 1) {
+#pragma unroll
+        for (int b = 0; b < MAXB; ++b) comb[b * kMrRows + row] = acc[b];
+    }
+    consumer_sync<kMrNC>();
+    if (h == 0) {
+#pragma unroll
+        for (int b = 0; b < MAXB; ++b) comb[(MAXB + b) * kMrRows + row] = acc[b] + comb[b * kMrRows + row];
+    }
+    consumer_sync<kMrNC>();
+    const int* pairs = p.r.pair_list + first;
+    const int outs = NMAT == 2 ? p.row_tile : kMrRows;
+    for (int i = tid; i < outs * nb; i += kMrNC) {
+        const int r = i % outs, b = i / outs;
+        const int64_t n = row0 + r;
+        if (n >= p.n) continue;
+        const float a0 = comb[(MAXB + b) * kMrRows + r];
+        const float out = NMAT == 2 ? silu_mul(a0, comb[(MAXB + b) * kMrRows + p.row_tile + r]) : a0;
+        p.y[static_cast<int64_t>(pairs[b]) * p.ldy + n] = out;
+    }
+    consumer_sync<kMrNC>();  // the next group overwrites xs, xsum and comb
+    return true;
+}
+
+template <int QT, int NMAT>
+__global__ void __launch_bounds__(kMrThreads, 1)
+    moe_rows_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
+                    const __grid_constant__ MoeRowsParams p) {
+    using R = MrCfg<QT>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
+    uint64_t* empty = full + R::ns;
+    if (threadIdx.x == 0) PHB_TRACE_EV(p.trace_id, 0);
+    pdl_launch_dependents();
+    pdl_wait();  // routing results (and, for the down pass, h) come from the previous kernels
+    if (threadIdx.x == 0) PHB_TRACE_EV(p.trace_id, 1);
+    const int slot = blockIdx.y;
+    if (slot >= *p.r.n_active) return;
+    const int e = p.r.act_expert[slot];
+    const int first = p.r.act_off[slot];
+    const int cnt = p.r.act_cnt[slot];
+    const int64_t row0 = static_cast<int64_t>(blockIdx.x) * p.row_tile;
+    if (row0 >= p.n) return;
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        for (int s = 0; s < R::ns; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kMrCW);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+    const int ngroups = (cnt + kMoeGroup - 1) / kMoeGroup;
+    if (tid >= kMrNC) {
+        if (tid == kMrNC) {
+            const uint64_t pol = policy_evict_first();
+            constexpr int kElems = QT == 0 ? R::ub / 2 : R::ub;
+            int s = 0, issued = 0;
+            bool ok = true;
+            for (int gi = 0; gi < ngroups && ok; ++gi)
+                for (int u = 0; u < p.units_row; ++u, ++s) {
+                    const int sl = s % R::ns;
+                    if (s >= R::ns && !mbar_wait(&empty[sl], ((s / R::ns) - 1) & 1, &g_dev_err)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[sl], static_cast<uint32_t>(R::stage_bytes));
+                    uint8_t* dst = smem + sl * R::stage_bytes;
+                    tma_load_3d_hint(dst, &tm0, u * kElems, static_cast<int>(row0), e, &full[sl], pol);
+                    if (NMAT == 2)
+                        tma_load_3d_hint(dst + p.row_tile * R::ub, &tm1, u * kElems, static_cast<int>(row0), e,
+                                         &full[sl], pol);
+                    ++issued;
+                }
+            for (int i = max(0, issued - R::ns); i < issued; ++i) mbar_wait(&full[i % R::ns], (i / R::ns) & 1, &g_dev_err);
+        }
+        return;
+    }
+    int s = 0;
+    for (int gi = 0; gi < ngroups; ++gi) {
+        const int nb = min(kMoeGroup, cnt - gi * kMoeGroup);
+        const int fp = first + gi * kMoeGroup;
+        bool ok;
+        if (nb == 1)
+            ok = moe_rows_group<QT, NMAT, 1>(p, row0, fp, nb, smem, full, empty, s);
+        else if (nb == 2)
+            ok = moe_rows_group<QT, NMAT, 2>(p, row0, fp, nb, smem, full, empty, s);
+        else
+            ok = moe_rows_group<QT, NMAT, 4>(p, row0, fp, nb, smem, full, empty, s);
+        if (!ok) return;
+    }
+    if (tid == 0) PHB_TRACE_EV(p.trace_id, 3);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 moe_encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// [E][rows][row bytes] expert-major matrix as a 3-D tensor; one box = one unit of `box_rows` rows of one expert.
+bool encode_expert_map(CUtensorMap* m, int qt, const void* w, int e, int64_t rows, int64_t k, int box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 encode = moe_encode_fn();
+    if (encode == nullptr) return false;
+    const int ub = qt == 0 ? Fmt<0>::unit_bytes : Fmt<1>::unit_bytes;
+    const int64_t row_bytes = k / kUnitWeights * ub;
+    const int esz = qt == 0 ? 2 : 1;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(row_bytes / esz), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(e)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows * row_bytes)};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(ub / esz), static_cast<cuuint32_t>(box_rows), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return encode(m, qt == 0 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(w),
+                  dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Shared-memory layout of the row-resident pass for K and the token group size.
+size_t moe_rows_layout(int qt, int64_t k, MoeRowsParams* p) {
+    const int ns = qt == 0 ? MrCfg<0>::ns : MrCfg<1>::ns;
+    const size_t stage = static_cast<size_t>(kMrRows) * (qt == 0 ? Fmt<0>::unit_bytes : Fmt<1>::unit_bytes);
+    const int kseg = static_cast<int>(k);
+    size_t off = ns * stage;
+    p->xs_off = static_cast<uint32_t>(off);
+    off += static_cast<size_t>(kMoeGroup) * xpad_len(kseg) * 4;
+    p->xsum_off = static_cast<uint32_t>(off);
+    off += static_cast<size_t>(kMoeGroup) * (kseg / 32) * 4;
+    p->comb_off = static_cast<uint32_t>(off);
+    off += 2 * static_cast<size_t>(kMoeGroup) * kMrRows * 4;
+    off = (off + 15) & ~size_t{15};
+    p->bar_off = static_cast<uint32_t>(off);
+    off += 2 * ns * sizeof(uint64_t) + kTailFloats * sizeof(float);
+    return off;
+}
+
+template <int QT, int NMAT>
+cudaError_t launch_moe_rows(const CUtensorMap& t0, const CUtensorMap& t1, const MoeRowsParams& p, dim3 grid,
+                            size_t smem, cudaStream_t s) {
+    constexpr auto kern = moe_rows_kernel<QT, NMAT>;
+    cudaError_t e = ensure_smem_attr<kern>();
+    if (e != cudaSuccess) return e;
+    return launch_kernel(kern, grid, dim3(kMrThreads), smem, s, true, t0, t1, p);
 }
 
 struct MoeWs {
@@ -371,49 +497,6 @@ MoeWs moe_ws_layout(const MoeReq& q, void* base) {
     return w;
 }
 
-template <int QT, int NMAT>
-cudaError_t launch_moe_stream(const MoeParams& p, dim3 grid, size_t smem, cudaStream_t s) {
-    constexpr auto kern = moe_stream_kernel<QT, NMAT>;
-    cudaError_t e = ensure_smem_attr<kern>();
-    if (e != cudaSuccess) return e;
-    return launch_kernel(kern, grid, dim3(KCfg<QT, kMoeCW>::threads), smem, s, true, p);
-}
-
-// Rows per CTA and shared-memory layout of one grouped pass. `maxb` is the
-// largest token group (at most the token count). A CTA gets at most about 8
-// stages of weights per token group, and few enough rows that its row sums fit
-// the tile partials (the fold mode synchronises the CTA at every stage).
-bool plan_moe(int qt, int nmat, int64_t n, int64_t k, int cpe, int maxb, MoeParams* p, unsigned* gx,
-              size_t* smem) {
-    const int units_row = static_cast<int>(k / kUnitWeights);
-    int rows_per_cta = static_cast<int>(cdiv(n, cpe));
-    rows_per_cta = std::min(rows_per_cta, std::max(1, 8 * KCfg<0, kMoeCW>::stage_units / (nmat * units_row)));
-    SmemLayout lay{};
-    for (;;) {
-        lay = stream_smem_layout(qt, kMoeCW, nmat, maxb, rows_per_cta, units_row);
-        if (lay.total <= kSmemOptin && lay.sum_mode != kSumFold) break;
-        if (rows_per_cta == 1) {
-            if (lay.total <= kSmemOptin) break;
-            return false;
-        }
-        rows_per_cta = (rows_per_cta + 1) / 2;
-    }
-    p->units_row = units_row;
-    p->rows_per_cta = rows_per_cta;
-    p->row_bytes = static_cast<int64_t>(units_row) * (qt == 0 ? Fmt<0>::unit_bytes : Fmt<1>::unit_bytes);
-    p->n = n;
-    p->expert_stride = n * p->row_bytes;
-    p->sum_mode = lay.sum_mode;
-    p->xs_off = lay.xs;
-    p->xsum_off = lay.xsum;
-    p->part_off = lay.part;
-    p->acc_off = lay.acc;
-    p->bar_off = lay.bar;
-    *gx = static_cast<unsigned>(cdiv(n, rows_per_cta));
-    *smem = lay.total;
-    return true;
-}
-
 }  // namespace
 
 size_t moe_ws_bytes(const MoeReq& q) { return moe_ws_layout(q, nullptr).bytes; }
@@ -431,53 +514,52 @@ cudaError_t moe_run(const MoeReq& q, cudaStream_t s) {
     cudaError_t e = launch_kernel(moe_route_kernel, dim3(1), dim3(256), 0, s, true, q.logits, static_cast<int>(q.t),
                                   q.e, q.top_k, w.r, q.out_idx, q.out_p, tb);
     if (e != cudaSuccess) return e;
-    // CTAs per expert: enough to cover the GPU twice for the expected number
-    // of distinct experts, E * (1 - (1 - k/E)^T).
-    double expected = q.e * (1.0 - std::pow(1.0 - static_cast<double>(q.top_k) / q.e, static_cast<double>(q.t)));
-    expected = std::min<double>(slots, std::max(1.0, expected));
-    const int cpe = std::max(1, static_cast<int>(std::ceil(2.0 * device_sm_count() / expected)));
-
-    MoeParams pg{};
-    unsigned gx = 0;
-    size_t smem = 0;
-    // tokens per expert never exceed the token count: size the staged activations for that
-    const int maxb = maxb_for(static_cast<int>(std::min<int64_t>(kMoeGroup, q.t)));
-    if (!plan_moe(q.qt, 2, q.d_ff, q.d_model, cpe, maxb, &pg, &gx, &smem)) return cudaErrorInvalidConfiguration;
-    pg.w[0] = static_cast<const uint8_t*>(q.wg);
-    pg.w[1] = static_cast<const uint8_t*>(q.wu);
-    pg.x = q.x;
-    pg.ldx = q.d_model;
-    pg.x_by_pair = 0;
-    pg.top_k = q.top_k;
-    pg.y = w.h;
-    pg.ldy = q.d_ff;
-    pg.r = w.r;
-    pg.pf = static_cast<const uint8_t*>(q.wd);
-    pg.trace_id = tb + 1;
-    pg.pf_stride = q.d_model * static_cast<int64_t>(q.qt == 0 ? q.d_ff / 32 * 34 : q.d_ff / 256 * 144);
-    e = q.qt == 0 ? launch_moe_stream<0, 2>(pg, dim3(gx, slots), smem, s)
-                  : launch_moe_stream<1, 2>(pg, dim3(gx, slots), smem, s);
-    if (e != cudaSuccess) return e;
-
-    MoeParams pd{};
-    if (!plan_moe(q.qt, 1, q.d_model, q.d_ff, cpe, maxb, &pd, &gx, &smem)) return cudaErrorInvalidConfiguration;
-    pd.w[0] = pd.w[1] = static_cast<const uint8_t*>(q.wd);
-    pd.x = w.h;
-    pd.ldx = q.d_ff;
-    pd.x_by_pair = 1;
-    pd.top_k = q.top_k;
-    pd.y = w.yp;
-    pd.ldy = q.d_model;
-    pd.r = w.r;
-    pd.trace_id = tb + 2;
-    e = q.qt == 0 ? launch_moe_stream<0, 1>(pd, dim3(gx, slots), smem, s)
-                  : launch_moe_stream<1, 1>(pd, dim3(gx, slots), smem, s);
-    if (e != cudaSuccess) return e;
-
-    const int64_t total = q.t * q.d_model;
-    return launch_kernel(moe_combine_kernel, dim3(static_cast<unsigned>(cdiv(total, 256))), dim3(256), 0, s, true,
-                         static_cast<const float*>(w.yp), static_cast<const float*>(w.r.p), q.y,
-                         static_cast<int>(q.t), q.top_k, q.d_model, tb + 3);
+    // row-resident grouped passes (3-D TMA unit stages)
+    {
+        CUtensorMap tg, tu, td;
+        if (!encode_expert_map(&tg, q.qt, q.wg, q.e, q.d_ff, q.d_model, 64) ||
+            !encode_expert_map(&tu, q.qt, q.wu, q.e, q.d_ff, q.d_model, 64) ||
+            !encode_expert_map(&td, q.qt, q.wd, q.e, q.d_model, q.d_ff, kMrRows))
+            return cudaErrorInvalidValue;
+        MoeRowsParams pg{};
+        const size_t smem_g = moe_rows_layout(q.qt, q.d_model, &pg);
+        pg.x = q.x;
+        pg.ldx = q.d_model;
+        pg.x_by_pair = 0;
+        pg.top_k = q.top_k;
+        pg.y = w.h;
+        pg.ldy = q.d_ff;
+        pg.r = w.r;
+        pg.n = q.d_ff;
+        pg.units_row = static_cast<int>(q.d_model / kUnitWeights);
+        pg.row_tile = 64;
+        pg.trace_id = tb + 1;
+        if (smem_g > kSmemOptin) return cudaErrorInvalidConfiguration;
+        const dim3 gg(static_cast<unsigned>(cdiv(q.d_ff, 64)), static_cast<unsigned>(slots));
+        e = q.qt == 0 ? launch_moe_rows<0, 2>(tg, tu, pg, gg, smem_g, s) : launch_moe_rows<1, 2>(tg, tu, pg, gg, smem_g, s);
+        if (e != cudaSuccess) return e;
+        MoeRowsParams pd{};
+        const size_t smem_d = moe_rows_layout(q.qt, q.d_ff, &pd);
+        pd.x = w.h;
+        pd.ldx = q.d_ff;
+        pd.x_by_pair = 1;
+        pd.top_k = q.top_k;
+        pd.y = w.yp;
+        pd.ldy = q.d_model;
+        pd.r = w.r;
+        pd.n = q.d_model;
+        pd.units_row = static_cast<int>(q.d_ff / kUnitWeights);
+        pd.row_tile = kMrRows;
+        pd.trace_id = tb + 2;
+        if (smem_d > kSmemOptin) return cudaErrorInvalidConfiguration;
+        const dim3 gd(static_cast<unsigned>(cdiv(q.d_model, kMrRows)), static_cast<unsigned>(slots));
+        e = q.qt == 0 ? launch_moe_rows<0, 1>(td, td, pd, gd, smem_d, s) : launch_moe_rows<1, 1>(td, td, pd, gd, smem_d, s);
+        if (e != cudaSuccess) return e;
+        const int64_t total = q.t * q.d_model;
+        return launch_kernel(moe_combine_kernel, dim3(static_cast<unsigned>(cdiv(total, 256))), dim3(256), 0, s, true,
+                             static_cast<const float*>(w.yp), static_cast<const float*>(w.r.p), q.y,
+                             static_cast<int>(q.t), q.top_k, q.d_model, tb + 3);
+    }
 }
 
 }  // namespace phb
