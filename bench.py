@@ -293,7 +293,7 @@ def bench_moe(t_tokens, steps, seed):
     x = torch.from_numpy(synth.normal_f32(seed, 1, (t_tokens, d_model))).cuda()
     logits = [torch.from_numpy(synth.normal_f32(seed, 5000 + l, (t_tokens, e))).cuda() for l in range(n_layers)]
     y = torch.empty_like(x)
-    ws = phb.workspace(phb.moe_workspace_size("q4_k", t_tokens, d_model, d_ff, e, k))
+    ws = phb.moe_workspace("q4_k", t_tokens, d_model, d_ff, e, k)
     idx = torch.empty((t_tokens, k), dtype=torch.int32, device="cuda")
 
     def step(_):
@@ -437,7 +437,7 @@ def run_profile(args):
         x = torch.from_numpy(synth.normal_f32(seed, 1, (t_tokens, d_model))).cuda()
         logits = [torch.from_numpy(synth.normal_f32(seed, 5000 + l, (t_tokens, e))).cuda() for l in range(n_layers)]
         y = torch.empty_like(x)
-        ws = phb.workspace(phb.moe_workspace_size("q4_k", t_tokens, d_model, d_ff, e, top_k))
+        ws = phb.moe_workspace("q4_k", t_tokens, d_model, d_ff, e, top_k)
 
         def call():
             for l in range(n_layers):

@@ -138,9 +138,9 @@ phb_status phb_ffn_swiglu(int qtype, const void* Wgate, const void* Wup, const v
  * the top_k largest router logits (ties to the lower expert index) select
  * experts e_{t,k} with weights p_{t,k} = softmax over those top_k logits, and
  * Y[t] = sum_k p_{t,k} * FFN_{e_{t,k}}(X[t]) with FFN the SwiGLU block above.
- * Each active expert's weights are read once for all tokens routed to it;
- * the weighted sum runs in a fixed order (slot k ascending), so repeated
- * calls are bitwise identical.
+ * Each active expert's weights are read once per group of up to four
+ * tokens routed to it; the weighted sum runs in a fixed order (slot k
+ * ascending), so repeated calls are bitwise identical.
  * Wgate, Wup: [n_experts][d_ff][d_model]; Wdown: [n_experts][d_model][d_ff];
  * X: [n_tokens][d_model]; router_logits: [n_tokens][n_experts] fp32;
  * Y: [n_tokens][d_model]. out_idx ([n_tokens][top_k] int32) and out_p

@@ -7,4 +7,4 @@ is the thin torch binding.
 
 from .api import (Q4_K, Q8_0, PhbError, decode_step, decode_workspace, decode_workspace_size, dequant, device_error,  # noqa: F401
                   ffn_swiglu, ffn_workspace_size, gemm_q_prefill, gemv, gemv_workspace_size, layer_table,
-                  moe_ffn, moe_workspace_size, prefill_workspace_size, row_bytes, workspace)
+                  moe_ffn, moe_workspace, moe_workspace_size, prefill_workspace_size, row_bytes, workspace)

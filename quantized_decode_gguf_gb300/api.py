@@ -135,6 +135,12 @@ def moe_workspace_size(qtype, n_tokens: int, d_model: int, d_ff: int, n_experts:
     return int(_lib.load().phb_moe_ffn_workspace_size(qtype_id(qtype), n_tokens, d_model, d_ff, n_experts, top_k))
 
 
+def moe_workspace(qtype, n_tokens: int, d_model: int, d_ff: int, n_experts: int, top_k: int, device=None):
+    """Workspace for :func:`moe_ffn` (zero-filled), reusable across calls."""
+    n = moe_workspace_size(qtype, n_tokens, d_model, d_ff, n_experts, top_k)
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+
+
 def moe_ffn(qtype, w_gate, w_up, w_down, x: torch.Tensor, logits: torch.Tensor, d_model: int, d_ff: int,
             n_experts: int, top_k: int, out: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
             out_idx: Optional[torch.Tensor] = None, out_p: Optional[torch.Tensor] = None) -> torch.Tensor:
@@ -143,7 +149,7 @@ def moe_ffn(qtype, w_gate, w_up, w_down, x: torch.Tensor, logits: torch.Tensor, 
     if out is None:
         out = torch.empty((t, d_model), dtype=torch.float32, device=x.device)
     if ws is None:
-        ws = workspace(moe_workspace_size(qt, t, d_model, d_ff, n_experts, top_k), x.device)
+        ws = moe_workspace(qt, t, d_model, d_ff, n_experts, top_k, x.device)
     _check(_lib.load().phb_moe_ffn(qt, _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(x), _ptr(logits), _ptr(out), t,
                                    d_model, d_ff, n_experts, top_k, _ptr(out_idx), _ptr(out_p), _ptr(ws), ws.numel(),
                                    _stream()))

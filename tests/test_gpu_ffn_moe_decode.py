@@ -89,7 +89,9 @@ MOE_CASES = [
     ("q4_k", 16, 128, 8, 2048, 768),   # 16 tokens per step
     ("q4_k", 5, 8, 2, 256, 512),
     ("q8_0", 7, 16, 4, 512, 256),
-    ("q4_k", 64, 32, 8, 256, 256),     # many tokens per expert (groups of 8)
+    ("q4_k", 64, 32, 8, 256, 256),     # many tokens per expert (groups of 4)
+    ("q8_0", 1, 16, 4, 512, 256),      # one token, other shapes
+    ("q4_k", 1, 8, 2, 256, 512),
 ]
 
 
@@ -140,6 +142,30 @@ def test_moe_one_hot_equals_ffn_and_is_deterministic():
                                         oracle.dequant(qtype, wd[c], d_model, d_ff), x[ti:ti + 1])
         assert_within(y[ti], ref[0], tol[0], "one-hot moe")
         assert_within(yf[0], ref[0], tol[0], "ffn")
+
+
+def test_moe_one_token_repeats_through_one_workspace_and_graph():
+    # calls and CUDA-graph replays through one workspace give the same bits
+    qtype, e, k, d_model, d_ff = "q4_k", 32, 4, 512, 512
+    wg, wu, wd = (to_dev(a) for a in _experts(qtype, 540, e, d_model, d_ff))
+    ws = phb.moe_workspace(qtype, 1, d_model, d_ff, e, k)
+    x = to_dev(synth.normal_f32(540, 1, (1, d_model)))
+    lg = to_dev(synth.normal_f32(540, 2, (1, e)))
+    y = torch.empty_like(x)
+    first = to_host(phb.moe_ffn(qtype, wg, wu, wd, x, lg, d_model, d_ff, e, k, out=y, ws=ws)).copy()
+    for _ in range(3):
+        assert np.array_equal(to_host(phb.moe_ffn(qtype, wg, wu, wd, x, lg, d_model, d_ff, e, k, out=y, ws=ws)),
+                              first)
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        phb.moe_ffn(qtype, wg, wu, wd, x, lg, d_model, d_ff, e, k, out=y, ws=ws)
+    for i in range(3):
+        y.zero_()
+        g.replay()
+        assert np.array_equal(to_host(y), first), i
+    check_device_clean()
 
 
 def test_moe_all_logits_equal_picks_lowest_experts():
