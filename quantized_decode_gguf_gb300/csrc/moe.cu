@@ -1,9 +1,11 @@
 // Top-k routed mixture-of-experts FFN.
 //
-// 1. moe_route_kernel (one CTA): per token the top_k largest router logits
-//    (ties to the lower expert index) and their softmax; then a counting sort
-//    of the (token, slot) pairs by expert, ascending pair id within an
-//    expert, giving the active-expert list.
+// 1. Routing (for one or two tokens in every CTA of the gate/up pass, CTA
+//    (0, 0) publishing it; for more tokens in a one-CTA kernel):
+//    per token the top_k largest router logits (ties to the lower expert
+//    index) and their softmax; then a counting sort of the (token, slot)
+//    pairs by expert, ascending pair id within an expert, giving the
+//    active-expert list.
 // 2. moe_rows_kernel<NMAT=2>: grid (row tiles of 64, expert slot). Each CTA
 //    streams 64 rows of its expert's gate and up matrices (one 3-D TMA copy
 //    per matrix and 256-weight unit) once per group of up to four tokens
@@ -76,27 +78,33 @@ __device__ __forceinline__ float key_float(uint32_t k) {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-// Routing. Warps take tokens; per token, K rounds of a warp-wide arg-max
-// (largest logit, then lowest expert index) over the logits held in
-// registers give the top_k in slot order, and lane 0 takes their softmax.
-// Then warp 0 sorts the (token, slot) pairs by expert with a stable
-// counting sort (match groups per 32 pairs, a warp scan over the experts)
-// and lists the active experts in ascending order.
-__global__ void __launch_bounds__(256) moe_route_kernel(const float* __restrict__ logits, int T, int E, int K,
-                                                        RouteOut o, int32_t* out_idx, float* out_p, int trace_id) {
-    (void)trace_id;
-    if (threadIdx.x == 0) PHB_TRACE_EV(trace_id, 0);
-    pdl_launch_dependents();
-    pdl_wait();
-    if (threadIdx.x == 0) PHB_TRACE_EV(trace_id, 1);
-    __shared__ int32_t sidx[kMaxTokens * kMaxTopK];
-    __shared__ int32_t rank[kMaxTokens * kMaxTopK];
-    __shared__ int32_t cnt[kMaxExperts];
-    __shared__ int32_t off[kMaxExperts];
+// Routing state in shared memory.
+struct RouteSm {
+    int32_t sidx[kMaxTokens * kMaxTopK];
+    int32_t rank[kMaxTokens * kMaxTopK];
+    int32_t cnt[kMaxExperts];
+    int32_t off[kMaxExperts];
+    int32_t act_expert[kMaxExperts];
+    int32_t act_off[kMaxExperts];
+    int32_t act_cnt[kMaxExperts];
+    int32_t pair_list[kMaxTokens * kMaxTopK];
+    int32_t n_active;
+};
+
+// Routing by 256 threads (the CTA's consumers; named barrier 1). Warps take
+// tokens; per token, K rounds of a warp-wide arg-max (largest logit, then
+// lowest expert index) over the logits held in registers give the top_k in
+// slot order, and lane 0 takes their softmax. Then warp 0 sorts the
+// (token, slot) pairs by expert with a stable counting sort (match groups
+// per 32 pairs, a warp scan over the experts) and lists the active experts
+// in ascending order. Everything lands in `sm`; with `go` non-null the
+// lists, indices and weights are also written to global memory.
+__device__ __forceinline__ void route_block(const float* __restrict__ logits, int T, int E, int K, RouteSm* sm,
+                                            const RouteOut* go, int32_t* out_idx, float* out_p) {
+    constexpr int NT = 256;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nwarps = blockDim.x >> 5;
-    for (int e = tid; e < kMaxExperts; e += blockDim.x) cnt[e] = 0;
-    for (int t = warp; t < T; t += nwarps) {
+    for (int e = tid; e < kMaxExperts; e += NT) sm->cnt[e] = 0;
+    for (int t = warp; t < T; t += NT / 32) {
         uint32_t key[kMaxExperts / 32];
 #pragma unroll
         for (int j = 0; j < kMaxExperts / 32; ++j) {
@@ -141,28 +149,30 @@ __global__ void __launch_bounds__(256) moe_route_kernel(const float* __restrict_
                 if (r >= K) break;
                 const float pr = ex[r] / sum;
                 const int q = t * K + r;
-                sidx[q] = sel_e[r];
-                o.idx[q] = sel_e[r];
-                o.p[q] = pr;
-                if (out_idx) out_idx[q] = sel_e[r];
-                if (out_p) out_p[q] = pr;
+                sm->sidx[q] = sel_e[r];
+                if (go) {
+                    go->idx[q] = sel_e[r];
+                    go->p[q] = pr;
+                    if (out_idx) out_idx[q] = sel_e[r];
+                    if (out_p) out_p[q] = pr;
+                }
             }
         }
     }
-    __syncthreads();
+    consumer_sync<NT>();
     const int pairs = T * K;
     if (warp == 0) {
         // stable rank of every pair within its expert, 32 pairs at a time
         for (int q0 = 0; q0 < pairs; q0 += 32) {
             const int q = q0 + lane;
             const bool valid = q < pairs;
-            const int e = valid ? sidx[q] : -1 - lane;  // invalid lanes match nobody
+            const int e = valid ? sm->sidx[q] : -1 - lane;  // invalid lanes match nobody
             const unsigned grp = __match_any_sync(0xFFFFFFFFu, e);
-            const int base = valid ? cnt[e] : 0;
+            const int base = valid ? sm->cnt[e] : 0;
             __syncwarp();
             if (valid) {
-                rank[q] = base + __popc(grp & ((1u << lane) - 1u));
-                if ((__ffs(grp) - 1) == lane) cnt[e] = base + __popc(grp);
+                sm->rank[q] = base + __popc(grp & ((1u << lane) - 1u));
+                if ((__ffs(grp) - 1) == lane) sm->cnt[e] = base + __popc(grp);
             }
             __syncwarp();
         }
@@ -172,7 +182,7 @@ __global__ void __launch_bounds__(256) moe_route_kernel(const float* __restrict_
 #pragma unroll
         for (int i = 0; i < kPer; ++i) {
             const int e = kPer * lane + i;
-            c[i] = e < E ? cnt[e] : 0;
+            c[i] = e < E ? sm->cnt[e] : 0;
             lc += c[i];
             la += c[i] > 0;
         }
@@ -190,22 +200,47 @@ __global__ void __launch_bounds__(256) moe_route_kernel(const float* __restrict_
         for (int i = 0; i < kPer; ++i) {
             const int e = kPer * lane + i;
             if (e < E) {
-                off[e] = acc;
+                sm->off[e] = acc;
                 if (c[i] > 0) {
-                    o.act_expert[a] = e;
-                    o.act_off[a] = acc;
-                    o.act_cnt[a] = c[i];
+                    sm->act_expert[a] = e;
+                    sm->act_off[a] = acc;
+                    sm->act_cnt[a] = c[i];
+                    if (go) {
+                        go->act_expert[a] = e;
+                        go->act_off[a] = acc;
+                        go->act_cnt[a] = c[i];
+                    }
                     ++a;
                 }
                 acc += c[i];
             }
         }
-        if (lane == 31) *o.n_active = sa;
+        if (lane == 31) {
+            sm->n_active = sa;
+            if (go) *go->n_active = sa;
+        }
     }
-    __syncthreads();
-    for (int q = tid; q < pairs; q += blockDim.x) o.pair_list[off[sidx[q]] + rank[q]] = q;
-    if (threadIdx.x == 0) PHB_TRACE_EV(trace_id, 3);
+    consumer_sync<NT>();
+    for (int q = tid; q < pairs; q += NT) {
+        const int w = sm->off[sm->sidx[q]] + sm->rank[q];
+        sm->pair_list[w] = q;
+        if (go) go->pair_list[w] = q;
+    }
+    consumer_sync<NT>();
 }
+
+// Routing as its own one-CTA kernel (used when many tokens would make every
+// gate/up CTA sort all pairs itself).
+__global__ void __launch_bounds__(256) moe_route_kernel(const float* __restrict__ logits, int T, int E, int K,
+                                                        RouteOut o, int32_t* out_idx, float* out_p) {
+    __shared__ RouteSm sm;
+    pdl_launch_dependents();
+    pdl_wait();
+    route_block(logits, T, E, K, &sm, &o, out_idx, out_p);
+}
+
+// Token counts up to which every gate/up CTA routes the tokens itself.
+constexpr int kMoeInlineRouteTokens = 2;
 
 __global__ void __launch_bounds__(256) moe_combine_kernel(const float* __restrict__ yp, const float* __restrict__ p,
                                                           float* __restrict__ y, int T, int K, int64_t D,
@@ -254,8 +289,14 @@ struct MoeRowsParams {
     int64_t n;             // rows per expert matrix
     int units_row;
     int row_tile;          // rows of each matrix per CTA: 64 (gate/up) or 128 (down)
-    uint32_t xs_off, xsum_off, comb_off, bar_off;
+    uint32_t xs_off, xsum_off, comb_off, bar_off, route_off;
     int trace_id;
+    // gate/up pass: the routing is computed in the kernel from the logits
+    const float* logits;
+    int n_tokens, n_experts;
+    int32_t* out_idx;
+    float* out_p;
+    int route_inline;  // gate/up pass: 1 = route in the kernel, 0 = read the routing kernel's lists
 };
 
 __device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* map, int x, int y, int z,
@@ -271,8 +312,8 @@ __device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* m
 // activations, stream every unit, write silu(gate) * up (NMAT 2) or the row
 // sums (NMAT 1) for each token.
 template <int QT, int NMAT, int MAXB>
-__device__ __forceinline__ bool moe_rows_group(const MoeRowsParams& p, int64_t row0, int first, int nb, uint8_t* smem,
-                                               uint64_t* full, uint64_t* empty, int& s) {
+__device__ __forceinline__ bool moe_rows_group(const MoeRowsParams& p, const int32_t* plist, int64_t row0, int first,
+                                               int nb, uint8_t* smem, uint64_t* full, uint64_t* empty, int& s) {
     using R = MrCfg<QT>;
     float* xs = reinterpret_cast<float*>(smem + p.xs_off);
     float* xsum = reinterpret_cast<float*>(smem + p.xsum_off);
@@ -283,7 +324,7 @@ __device__ __forceinline__ bool moe_rows_group(const MoeRowsParams& p, int64_t r
     const int tid = threadIdx.x, lane = tid & 31;
     const int kseg = p.units_row * kUnitWeights;
     if (tid < nb) {
-        const int pair = p.r.pair_list[first + tid];
+        const int pair = plist[first + tid];
         rowidx[tid] = p.x_by_pair ? pair : pair / p.top_k;
     }
     consumer_sync<kMrNC>();
@@ -322,7 +363,7 @@ __device__ __forceinline__ bool moe_rows_group(const MoeRowsParams& p, int64_t r
         for (int b = 0; b < MAXB; ++b) comb[(MAXB + b) * kMrRows + row] = acc[b] + comb[b * kMrRows + row];
     }
     consumer_sync<kMrNC>();
-    const int* pairs = p.r.pair_list + first;
+    const int* pairs = plist + first;
     const int outs = NMAT == 2 ? p.row_tile : kMrRows;
     for (int i = tid; i < outs * nb; i += kMrNC) {
         const int r = i % outs, b = i / outs;
@@ -346,13 +387,33 @@ __global__ void __launch_bounds__(kMrThreads, 1)
     uint64_t* empty = full + R::ns;
     if (threadIdx.x == 0) PHB_TRACE_EV(p.trace_id, 0);
     pdl_launch_dependents();
-    pdl_wait();  // routing results (and, for the down pass, h) come from the previous kernels
+    pdl_wait();  // x and the logits (gate/up), or the routing and h (down), come from earlier kernels
     if (threadIdx.x == 0) PHB_TRACE_EV(p.trace_id, 1);
+    const int32_t* act_expert = p.r.act_expert;
+    const int32_t* act_off = p.r.act_off;
+    const int32_t* act_cnt = p.r.act_cnt;
+    const int32_t* plist = p.r.pair_list;
+    int n_active;
+    if (NMAT == 2 && p.route_inline) {
+        // every CTA routes the tokens itself; CTA (0, 0) publishes the result for the later passes
+        RouteSm* rs = reinterpret_cast<RouteSm*>(smem + p.route_off);
+        if (threadIdx.x < kMrNC)
+            route_block(p.logits, p.n_tokens, p.n_experts, p.top_k, rs,
+                        (blockIdx.x == 0 && blockIdx.y == 0) ? &p.r : nullptr, p.out_idx, p.out_p);
+        __syncthreads();
+        act_expert = rs->act_expert;
+        act_off = rs->act_off;
+        act_cnt = rs->act_cnt;
+        plist = rs->pair_list;
+        n_active = rs->n_active;
+    } else {
+        n_active = *p.r.n_active;
+    }
     const int slot = blockIdx.y;
-    if (slot >= *p.r.n_active) return;
-    const int e = p.r.act_expert[slot];
-    const int first = p.r.act_off[slot];
-    const int cnt = p.r.act_cnt[slot];
+    if (slot >= n_active) return;
+    const int e = act_expert[slot];
+    const int first = act_off[slot];
+    const int cnt = act_cnt[slot];
     const int64_t row0 = static_cast<int64_t>(blockIdx.x) * p.row_tile;
     if (row0 >= p.n) return;
     const int tid = threadIdx.x;
@@ -396,11 +457,11 @@ __global__ void __launch_bounds__(kMrThreads, 1)
         const int fp = first + gi * kMoeGroup;
         bool ok;
         if (nb == 1)
-            ok = moe_rows_group<QT, NMAT, 1>(p, row0, fp, nb, smem, full, empty, s);
+            ok = moe_rows_group<QT, NMAT, 1>(p, plist, row0, fp, nb, smem, full, empty, s);
         else if (nb == 2)
-            ok = moe_rows_group<QT, NMAT, 2>(p, row0, fp, nb, smem, full, empty, s);
+            ok = moe_rows_group<QT, NMAT, 2>(p, plist, row0, fp, nb, smem, full, empty, s);
         else
-            ok = moe_rows_group<QT, NMAT, 4>(p, row0, fp, nb, smem, full, empty, s);
+            ok = moe_rows_group<QT, NMAT, 4>(p, plist, row0, fp, nb, smem, full, empty, s);
         if (!ok) return;
     }
     if (tid == 0) PHB_TRACE_EV(p.trace_id, 3);
@@ -449,6 +510,9 @@ size_t moe_rows_layout(int qt, int64_t k, MoeRowsParams* p) {
     off += static_cast<size_t>(kMoeGroup) * (kseg / 32) * 4;
     p->comb_off = static_cast<uint32_t>(off);
     off += 2 * static_cast<size_t>(kMoeGroup) * kMrRows * 4;
+    off = (off + 15) & ~size_t{15};
+    p->route_off = static_cast<uint32_t>(off);
+    off += sizeof(RouteSm);
     off = (off + 15) & ~size_t{15};
     p->bar_off = static_cast<uint32_t>(off);
     off += 2 * ns * sizeof(uint64_t) + kTailFloats * sizeof(float);
@@ -511,9 +575,13 @@ cudaError_t moe_run(const MoeReq& q, cudaStream_t s) {
 #endif
     const int pairs = static_cast<int>(q.t * q.top_k);
     const int slots = std::min(q.e, pairs);
-    cudaError_t e = launch_kernel(moe_route_kernel, dim3(1), dim3(256), 0, s, true, q.logits, static_cast<int>(q.t),
-                                  q.e, q.top_k, w.r, q.out_idx, q.out_p, tb);
-    if (e != cudaSuccess) return e;
+    cudaError_t e;
+    const bool inline_route = q.t <= kMoeInlineRouteTokens;
+    if (!inline_route) {
+        e = launch_kernel(moe_route_kernel, dim3(1), dim3(256), 0, s, true, q.logits, static_cast<int>(q.t), q.e,
+                          q.top_k, w.r, q.out_idx, q.out_p);
+        if (e != cudaSuccess) return e;
+    }
     // row-resident grouped passes (3-D TMA unit stages)
     {
         CUtensorMap tg, tu, td;
@@ -534,6 +602,12 @@ cudaError_t moe_run(const MoeReq& q, cudaStream_t s) {
         pg.units_row = static_cast<int>(q.d_model / kUnitWeights);
         pg.row_tile = 64;
         pg.trace_id = tb + 1;
+        pg.logits = q.logits;
+        pg.n_tokens = static_cast<int>(q.t);
+        pg.n_experts = q.e;
+        pg.out_idx = q.out_idx;
+        pg.out_p = q.out_p;
+        pg.route_inline = inline_route ? 1 : 0;
         if (smem_g > kSmemOptin) return cudaErrorInvalidConfiguration;
         const dim3 gg(static_cast<unsigned>(cdiv(q.d_ff, 64)), static_cast<unsigned>(slots));
         e = q.qt == 0 ? launch_moe_rows<0, 2>(tg, tu, pg, gg, smem_g, s) : launch_moe_rows<1, 2>(tg, tu, pg, gg, smem_g, s);
