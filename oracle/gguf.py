@@ -35,6 +35,8 @@ Readings where the pages are silent (each is listed in the design notes):
   even) and multiplied exactly, accumulated in fp32.
 * Decode layer: RMSNorm without gain, eps = 1e-6; position 0, so attention
   returns V, query head h reads KV head h // (n_q / n_kv); residual adds.
+* Decode attention at context depth: fp16 KV cache [L][n_kv][head_dim], fp32
+  query and output, scaled dot-product softmax with scale 1/sqrt(head_dim).
 
 Exactness arguments used for bit-exact dequantisation:
 
@@ -317,6 +319,53 @@ def attention_pos0(qkv: np.ndarray, n_q_heads: int, n_kv_heads: int, head_dim: i
     v = qkv[:, v0:v0 + n_kv_heads * head_dim].reshape(qkv.shape[0], n_kv_heads, head_dim)
     heads = [v[:, h // group, :] for h in range(n_q_heads)]
     return np.concatenate(heads, axis=1)
+
+
+def attention_decode(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, n_q_heads: int, n_kv_heads: int,
+                     head_dim: int, scale: float | None = None):
+    """Attention of one decoding token over ``L`` cached positions.
+
+    Phobos README: ``phobos-bench -d N`` runs generation with N tokens
+    already in the context; ``phobos-kbench``'s ``flash_fp16`` kernel keeps
+    Q/K/V/O in f16 with an f32 online-softmax state; the ``kv_check``
+    example checks one decode step using the KV cache against a full
+    recompute. Readings: the cache is fp16 (as ``flash_fp16``), the query
+    and the output fp32 (as the rest of the decode path), grouped-query
+    heads (query head h reads KV head h // (n_q / n_kv)) and the usual
+    scaled dot-product softmax, scale = 1 / sqrt(head_dim) by default:
+
+        s_j = scale * q_h . k_j,   p = softmax(s),   out_h = sum_j p_j v_j
+
+    ``q``: [n_q, head_dim]; ``k_cache``, ``v_cache``: [L, n_kv, head_dim]
+    (fp16 values are exact in float64). Returns ``(out, tol)`` in float64:
+    ``tol`` bounds an fp32 evaluation (scores, exp and the sums in fp32, in
+    any order):
+
+        tol = A * (4 * ds + (L + head_dim + 16) * 2^-22),
+        A = sum_j p_j |v_j|,   ds = scale * head_dim * 2^-23 * max_j sum_d |q_d k_jd|
+
+    (a first-order bound: a score error ds moves every p_j by at most
+    2 p_j ds; each fp32 sum of n terms is within n * 2^-24 of exact).
+    """
+    qf = np.asarray(q, dtype=np.float64).reshape(n_q_heads, head_dim)
+    k = np.asarray(k_cache, dtype=np.float64).reshape(-1, n_kv_heads, head_dim)
+    v = np.asarray(v_cache, dtype=np.float64).reshape(-1, n_kv_heads, head_dim)
+    length = k.shape[0]
+    if scale is None:
+        scale = 1.0 / np.sqrt(head_dim)
+    group = n_q_heads // n_kv_heads
+    out = np.zeros((n_q_heads, head_dim))
+    tol = np.zeros((n_q_heads, head_dim))
+    for h in range(n_q_heads):
+        kv = h // group
+        s = scale * (k[:, kv, :] @ qf[h])
+        e = np.exp(s - s.max())
+        p = e / e.sum()
+        out[h] = p @ v[:, kv, :]
+        a = p @ np.abs(v[:, kv, :])
+        ds = scale * head_dim * 2.0 ** -23 * np.max(np.abs(k[:, kv, :]) @ np.abs(qf[h]))
+        tol[h] = a * (4.0 * ds + (length + head_dim + 16) * 2.0 ** -22)
+    return out, tol
 
 
 def _rmsnorm_bound(x: np.ndarray, dx: np.ndarray, eps_norm: float, eps: float = RMS_EPS):

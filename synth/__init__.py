@@ -103,3 +103,8 @@ SEED_BASE = 0x5EED0000
 
 def workload_seed(n: int) -> int:
     return SEED_BASE + int(n)
+
+
+def normal_f16(seed: int, tensor_id: int, shape) -> np.ndarray:
+    """N(0, 1) values rounded to fp16 (round to nearest even), e.g. a KV cache."""
+    return normal_f32(seed, tensor_id, shape).astype(np.float16)

@@ -290,3 +290,73 @@ def test_decode_layer_brute_force_python():
     want = [a + b for a, b in zip(x1, mv(wd, act))]
     assert np.allclose(x2[0], want, rtol=1e-12, atol=1e-12)
     assert np.all(dx2 > 0)
+
+
+# ---------------------------------------------------------------- decode attention at context depth
+
+def _attn_inputs(seed, length, n_q, n_kv, hd):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((n_q, hd)).astype(np.float32)
+    k = rng.standard_normal((length, n_kv, hd)).astype(np.float16)
+    v = rng.standard_normal((length, n_kv, hd)).astype(np.float16)
+    return q, k, v
+
+
+def test_attention_single_position_returns_v_exactly():
+    # one key: the softmax weight is exactly 1, so every query head returns its KV head's V
+    q, k, v = _attn_inputs(1, 1, 8, 2, 16)
+    out, tol = oracle.attention_decode(q, k, v, 8, 2, 16)
+    for h in range(8):
+        assert np.array_equal(out[h], v[0, h // 4].astype(np.float64))
+    assert np.all(tol >= 0)
+
+
+def test_attention_equal_keys_average_the_values():
+    # identical keys (or a zero query): uniform weights, the plain mean of V
+    q, k, v = _attn_inputs(2, 37, 4, 4, 8)
+    k[:] = k[0]
+    out, _ = oracle.attention_decode(q, k, v, 4, 4, 8)
+    assert np.allclose(out, v.astype(np.float64).mean(axis=0), rtol=1e-13, atol=1e-15)
+    out0, _ = oracle.attention_decode(np.zeros_like(q), *_attn_inputs(3, 37, 4, 4, 8)[1:], 4, 4, 8)
+    v3 = _attn_inputs(3, 37, 4, 4, 8)[2].astype(np.float64)
+    assert np.allclose(out0, v3.mean(axis=0), rtol=1e-13, atol=1e-15)
+
+
+def test_attention_dominant_key_selects_its_value():
+    q, k, v = _attn_inputs(4, 50, 2, 1, 8)
+    k[17, 0] = (40.0 * q[0]).astype(np.float16)  # score ~ 40 * |q|^2 / sqrt(8) dominates for head 0
+    out, _ = oracle.attention_decode(q, k, v, 2, 1, 8)
+    assert np.allclose(out[0], v[17, 0].astype(np.float64), rtol=0, atol=1e-12)
+
+
+def test_attention_matches_pure_python_brute_force():
+    q, k, v = _attn_inputs(5, 5, 4, 2, 3)
+    out, _ = oracle.attention_decode(q, k, v, 4, 2, 3, scale=0.7)
+    for h in range(4):
+        kv = h // 2
+        s = [0.7 * sum(float(q[h, d]) * float(k[j, kv, d]) for d in range(3)) for j in range(5)]
+        m = max(s)
+        e = [math.exp(x - m) for x in s]
+        z = sum(e)
+        for d in range(3):
+            want = sum(e[j] / z * float(v[j, kv, d]) for j in range(5))
+            assert abs(out[h, d] - want) <= 1e-14 * max(1.0, abs(want))
+
+
+def test_attention_invariances():
+    q, k, v = _attn_inputs(6, 33, 4, 2, 8)
+    out, _ = oracle.attention_decode(q, k, v, 4, 2, 8)
+    # scaling the query and dividing the scale by the same factor changes nothing
+    out2, _ = oracle.attention_decode(2.0 * q, k, v, 4, 2, 8, scale=0.5 / math.sqrt(8))
+    assert np.allclose(out, out2, rtol=1e-12, atol=1e-14)
+    # permuting the cached positions changes nothing
+    perm = np.random.default_rng(7).permutation(33)
+    out3, _ = oracle.attention_decode(q, k[perm], v[perm], 4, 2, 8)
+    assert np.allclose(out, out3, rtol=1e-12, atol=1e-14)
+    # grouped heads: changing KV head 1 leaves query heads 0 and 1 alone
+    k4, v4 = k.copy(), v.copy()
+    k4[:, 1] = 0
+    v4[:, 1] = 1
+    out4, _ = oracle.attention_decode(q, k4, v4, 4, 2, 8)
+    assert np.array_equal(out[:2], out4[:2])
+    assert np.allclose(out4[2:], 1.0)
