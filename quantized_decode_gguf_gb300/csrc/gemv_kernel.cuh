@@ -469,11 +469,6 @@ __global__ void __launch_bounds__(KCfg<QT, CW>::threads, MAXB <= 2 ? 2 : 1)
     uint64_t* empty = full + C::ns;
     float* xfac = reinterpret_cast<float*>(empty + C::ns);
     float* red = xfac + kAccStride;
-#ifdef PHB_EXP_XFIRST
-    // experiment: a barrier (in the unused row-list slot) that holds the weight
-    // copies back until the activations are staged
-    uint64_t* xready = reinterpret_cast<uint64_t*>(red + (2 * kMaxConsumerWarps + 3) * kAccStride);
-#endif
 
     const int tid = threadIdx.x;
     if (tid == 0) PHB_TRACE_EV(p.trace_id, 0);
@@ -500,9 +495,6 @@ __global__ void __launch_bounds__(KCfg<QT, CW>::threads, MAXB <= 2 ? 2 : 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], CW);
         }
-#ifdef PHB_EXP_XFIRST
-        mbar_init(xready, 1);
-#endif
         fence_barrier_init();
     }
     if (p.sum_mode == kSumFold)
@@ -513,15 +505,10 @@ __global__ void __launch_bounds__(KCfg<QT, CW>::threads, MAXB <= 2 ? 2 : 1)
         if (tid == C::consumers) {
             int s = 0;
             const uint64_t pol = policy_evict_first();
-#ifdef PHB_EXP_XFIRST
-            mbar_wait(xready, 0, &g_dev_err);
-#endif
             produce_tile<QT, CW>(t, NMAT, smem, full, empty, s, pol);
         } else if (tid == C::consumers + 1) {
-#ifndef PHB_NO_L2PF
             prefetch_share(p.pf[0], p.pf_bytes[0]);
             prefetch_share(p.pf[1], p.pf_bytes[1]);
-#endif
         }
         return;
     }
@@ -531,9 +518,6 @@ __global__ void __launch_bounds__(KCfg<QT, CW>::threads, MAXB <= 2 ? 2 : 1)
     stage_x<CW, MAXB, XMODE>(p.x, p.ldx, static_cast<int64_t>(u0) * kUnitWeights, kseg, batch, xs, xsum, xfac, red,
                              p.gather_group, p.gather_hd, p.gather_v_off);
     if (tid == 0) PHB_TRACE_EV(p.trace_id, 2);
-#ifdef PHB_EXP_XFIRST
-    if (tid == 0) mbar_arrive(xready);
-#endif
     const bool split_out = gridDim.y > 1;
     auto epi = [&](int r, int b, float a0, float a1) {
         const int64_t n = row0 + r;

@@ -46,12 +46,9 @@ struct SmemLayout {
 
 constexpr size_t kTilePartBudget = 48 * 1024;
 
-#ifndef PHB_CTAS_PER_SM
-#define PHB_CTAS_PER_SM 2
-#endif
 // CTAs of one GEMV per SM. Two half-SM CTAs measured fastest for the chained
 // decode GEMVs (a 24-layer Q8_0 step: 550 us with 2, 775 us with 1).
-constexpr int kCtasPerSm = PHB_CTAS_PER_SM;
+constexpr int kCtasPerSm = 2;
 
 inline SmemLayout stream_smem_layout(int qt, int cw, int nmat, int maxb, int rows_per_cta, int units_seg,
                                      int ring_stages = 0) {
