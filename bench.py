@@ -331,6 +331,36 @@ def bench_prefill(qtype, n, k, m, iters, seed, peaks):
             "frac_of_bf16_peak": tf / peaks["bf16_tflops"]}
 
 
+ATTN_SHAPE = (16, 4, 128)  # query heads, KV heads, head size of the dense decode workload
+
+
+def attention_inputs(n_ctx, seed):
+    import torch
+    n_q, n_kv, hd = ATTN_SHAPE
+    q = torch.from_numpy(synth.normal_f32(seed, 0, (n_q, hd))).cuda()
+    k = torch.from_numpy(synth.normal_f16(seed, 1, (n_ctx, n_kv, hd))).cuda()
+    v = torch.from_numpy(synth.normal_f16(seed, 2, (n_ctx, n_kv, hd))).cuda()
+    return q, k, v
+
+
+def bench_attention(n_ctx, iters, seed, l2, peaks):
+    """Decode attention of one token at context depth n_ctx (fp16 KV cache); GB/s of algorithmic bytes."""
+    import torch
+    import quantized_decode_gguf_gb300 as phb
+    n_q, n_kv, hd = ATTN_SHAPE
+    q, k, v = attention_inputs(n_ctx, seed)
+    kv = rotate_copies(torch.stack([k, v]), 2 * l2 + 64 * 2 ** 20)
+    out = torch.empty((n_q, hd), device="cuda")
+    ws = phb.workspace(phb.attention_workspace_size(n_ctx, n_q, n_kv, hd))
+    ms = graph_time(lambda i: phb.attention_decode(q, kv[i % len(kv)][0], kv[i % len(kv)][1], n_ctx, n_q, n_kv, hd,
+                                                   out=out, ws=ws), len(kv), iters)
+    b = 2 * n_ctx * n_kv * hd * 2 + 2 * 4 * n_q * hd
+    gbs = b / (ms * 1e-3) / 1e9
+    return {"n_ctx": n_ctx, "n_q": n_q, "n_kv": n_kv, "head_dim": hd, "us": ms * 1e3, "bytes": b, "gbs": gbs,
+            "frac": gbs / peaks["hbm_gbs"], "launches_per_call": 2,
+            "l2": "rotating KV copies larger than L2"}
+
+
 # ----------------------------------------------------------------------------- CPU oracle baseline
 
 def cpu_baseline(budget_s=12.0):  # about 12 s of oracle work
@@ -443,6 +473,13 @@ def run_profile(args):
             for l in range(n_layers):
                 phb.moe_ffn("q4_k", *mats[l], x, logits[l], d_model, d_ff, e, top_k, out=y, ws=ws)
         what = f"MoE FFN Q4_K, {t_tokens} tokens, {n_layers} layers"
+    elif args.profile == "attention":
+        n_q, n_kv, hd = ATTN_SHAPE
+        q, k, v = attention_inputs(args.ctx, seed)
+        out = torch.empty((n_q, hd), device="cuda")
+        ws = phb.workspace(phb.attention_workspace_size(args.ctx, n_q, n_kv, hd))
+        call = lambda: phb.attention_decode(q, k, v, args.ctx, n_q, n_kv, hd, out=out, ws=ws)  # noqa: E731
+        what = f"decode attention, {args.ctx} positions, {n_q}q/{n_kv}kv x {hd}"
     else:
         n, k, m = 9728, 2560, 512
         w = torch.from_numpy(synth.blocks("q4_k", seed, 0, n, k)).cuda()
@@ -470,11 +507,12 @@ def main():
     ap.add_argument("--impl", default="phb", choices=["phb", "reference"])
     ap.add_argument("--headline-only", action="store_true", help="skip the extra rows")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["decode", "decode-unfused", "prefill", "moe1", "moe16", "gemv"],
+    ap.add_argument("--profile", choices=["decode", "decode-unfused", "prefill", "moe1", "moe16", "gemv", "attention"],
                     help="run only this path --steps times after --warmup calls (a small case for ncu) and print "
                          "one status line instead of the bench line")
     ap.add_argument("--layers", type=int, default=N_LAYERS, help="decode layers in --profile decode modes")
     ap.add_argument("--gemv", default="q4_k,9728,2560,4", help="--profile gemv case: qtype,n,k,batch")
+    ap.add_argument("--ctx", type=int, default=32768, help="--profile attention: context positions")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
@@ -571,6 +609,8 @@ def main():
         torch.cuda.empty_cache()
         rows["prefill"] = [bench_prefill(q, n, k, 512, 20, synth.workload_seed(4), peaks)
                            for q in ("q4_k", "q8_0") for (n, k) in [(9728, 2560), (2560, 9728)]]
+        torch.cuda.empty_cache()
+        rows["attention_decode"] = [bench_attention(n, 50, synth.workload_seed(5), l2, peaks) for n in (4096, 32768)]
         result["rows"] = rows
     if rank == 0:
         if not args.no_cpu_baseline:

@@ -221,6 +221,30 @@ phb_status phb_decode_step_unfused(int qtype, const phb_dense_layer* layers, int
                                    void* ws, size_t ws_bytes, phb_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Decode attention at context depth (Phobos README: `phobos-bench -d N`,
+ * decode with N tokens already in context; `phobos-kbench` `flash_fp16`,
+ * f16 K/V with an f32 online-softmax state; the `kv_check` example).
+ * One token's n_q_heads query heads against n_ctx cached positions:
+ *   s_j = scale * q_h . k_j,   out_h = sum_j softmax(s)_j v_j   (j < n_ctx)
+ * with query head h reading KV head h / (n_q_heads / n_kv_heads).
+ * q: [n_q_heads][head_dim] fp32; k_cache, v_cache: [n_ctx][n_kv_heads]
+ * [head_dim] IEEE fp16 (the first n_ctx positions of a cache in that
+ * layout); out: [n_q_heads][head_dim] fp32. scale is usually
+ * 1/sqrt(head_dim). Scores, exponentials and sums are fp32; the result is
+ * within the fp32 error bound of the exact softmax and bitwise identical
+ * across calls. K and V are read once (query heads past 8 per KV head
+ * re-read them from L2).
+ * Needs n_q_heads % n_kv_heads == 0, head_dim 64, 128 or 256 and
+ * 1 <= n_ctx <= 2^26; every pointer 16-byte aligned. The workspace holds
+ * one partial result per position chunk; its size depends on the current
+ * device's SM count. Nothing in it needs to start at zero.
+ * ------------------------------------------------------------------------- */
+size_t phb_attention_decode_workspace_size(int64_t n_ctx, int n_q_heads, int n_kv_heads, int head_dim);
+phb_status phb_attention_decode(const float* q, const void* k_cache, const void* v_cache, float* out,
+                                int64_t n_ctx, int n_q_heads, int n_kv_heads, int head_dim, float scale,
+                                void* ws, size_t ws_bytes, phb_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * SwiGLU feed-forward block that allocates nothing. The paper has no
  * counterpart; this is a convenience for callers that cannot allocate
  * device memory (a serving loop whose memory budget is fixed at start-up,

@@ -10,6 +10,7 @@ are uint8 tensors holding the GGUF blocks, rows contiguous.
 from __future__ import annotations
 
 import ctypes
+import math
 from typing import Optional, Sequence
 
 import torch
@@ -212,3 +213,27 @@ def decode_step(qtype, table, n_layers: int, d_model: int, n_q: int, n_kv: int, 
     _check(fn(qt, ctypes.cast(table, ctypes.c_void_p), n_layers, d_model, n_q, n_kv, head_dim, d_ff, _ptr(x_in),
               _ptr(x_out), _ptr(ws), ws.numel(), _stream()))
     return x_out
+
+
+# ---------------------------------------------------------------- decode attention
+
+def attention_workspace_size(n_ctx: int, n_q: int, n_kv: int, head_dim: int) -> int:
+    return int(_lib.load().phb_attention_decode_workspace_size(n_ctx, n_q, n_kv, head_dim))
+
+
+def attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, n_ctx: int, n_q: int, n_kv: int,
+                     head_dim: int, scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                     ws: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """phb_attention_decode: q [n_q, head_dim] fp32 against the first ``n_ctx``
+    positions of an fp16 cache [>= n_ctx, n_kv, head_dim]; returns [n_q, head_dim] fp32."""
+    if k_cache.dtype != torch.float16 or v_cache.dtype != torch.float16:
+        raise TypeError("the KV cache must be float16")
+    if out is None:
+        out = torch.empty((n_q, head_dim), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = workspace(attention_workspace_size(n_ctx, n_q, n_kv, head_dim), q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(head_dim)
+    _check(_lib.load().phb_attention_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), n_ctx, n_q, n_kv,
+                                            head_dim, float(scale), _ptr(ws), ws.numel(), _stream()))
+    return out

@@ -1,6 +1,7 @@
 // C ABI of libphb: argument validation, workspace sizing and dispatch.
 // Every check runs on the host before anything is launched, so a call that
 // returns an error has launched nothing.
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <algorithm>
@@ -207,14 +208,15 @@ phb_status phb_device_error(int* code) {
     phb_status st = check_device();
     if (st != PHB_OK) return st;
     PHB_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
-    int c[6] = {0, 0, 0, 0, 0, 0};
+    int c[7] = {0, 0, 0, 0, 0, 0, 0};
     PHB_CUDA(phb::read_dev_err_gemv(&c[0]), "read device error");
     PHB_CUDA(phb::read_dev_err_decode(&c[1]), "read device error");
     PHB_CUDA(phb::read_dev_err_moe(&c[2]), "read device error");
     PHB_CUDA(phb::read_dev_err_prefill(&c[3]), "read device error");
     PHB_CUDA(phb::read_dev_err_decode_persistent(&c[4]), "read device error");
     PHB_CUDA(phb::read_dev_err_gemv_rows(&c[5]), "read device error");
-    *code = c[0] | c[1] | c[2] | c[3] | c[4] | c[5];
+    PHB_CUDA(phb::read_dev_err_attention(&c[6]), "read device error");
+    *code = c[0] | c[1] | c[2] | c[3] | c[4] | c[5] | c[6];
     if (*code) return fail(PHB_ERR_DEVICE_TIMEOUT, "a kernel reported device error %d", *code);
     return ok();
 }
@@ -560,6 +562,38 @@ phb_status phb_decode_step_unfused(int qtype, const phb_dense_layer* layers, int
         set_pf(q, 4 * l + 3);
         PHB_CUDA(phb::decode_gemv_run(q, stream), "decode down launch");
     }
+    return ok();
+}
+
+// ---------------------------------------------------------------- decode attention
+static constexpr int64_t kAttnMaxCtx = int64_t{1} << 26;
+
+size_t phb_attention_decode_workspace_size(int64_t n_ctx, int n_q_heads, int n_kv_heads, int head_dim) {
+    if (n_ctx < 1 || n_ctx > kAttnMaxCtx || !phb::attention_shape_ok(n_q_heads, n_kv_heads, head_dim)) return 0;
+    return phb::attention_ws_bytes(n_q_heads, n_kv_heads, head_dim, n_ctx);
+}
+
+phb_status phb_attention_decode(const float* q, const void* k_cache, const void* v_cache, float* out, int64_t n_ctx,
+                                int n_q_heads, int n_kv_heads, int head_dim, float scale, void* ws, size_t ws_bytes,
+                                phb_stream_t stream) {
+    PHB_REQUIRE(q && k_cache && v_cache && out, PHB_ERR_INVALID_ARG, "null tensor pointer");
+    PHB_REQUIRE(n_ctx >= 1 && n_ctx <= kAttnMaxCtx, PHB_ERR_INVALID_ARG, "n_ctx must be 1..2^26 (got %lld)",
+                static_cast<long long>(n_ctx));
+    PHB_REQUIRE(n_q_heads >= 1 && n_kv_heads >= 1, PHB_ERR_INVALID_ARG, "head counts must be positive");
+    PHB_REQUIRE(n_q_heads % n_kv_heads == 0, PHB_ERR_SHAPE, "n_q_heads must be a multiple of n_kv_heads");
+    PHB_REQUIRE(head_dim == 64 || head_dim == 128 || head_dim == 256, PHB_ERR_SHAPE,
+                "head_dim must be 64, 128 or 256 (got %d)", head_dim);
+    PHB_REQUIRE(std::isfinite(scale), PHB_ERR_INVALID_ARG, "scale must be finite");
+    PHB_REQUIRE(aligned16(q) && aligned16(k_cache) && aligned16(v_cache) && aligned16(out) && aligned16(ws),
+                PHB_ERR_ALIGN, "tensors must be 16-byte aligned");
+    const size_t need = phb_attention_decode_workspace_size(n_ctx, n_q_heads, n_kv_heads, head_dim);
+    PHB_REQUIRE(ws && ws_bytes >= need, PHB_ERR_WORKSPACE, "workspace needs %zu bytes (got %zu)", need, ws_bytes);
+    phb_status st = check_device();
+    if (st != PHB_OK) return st;
+    const cudaError_t e = phb::attention_run(q, k_cache, v_cache, out, n_q_heads, n_kv_heads, head_dim, n_ctx, scale,
+                                             ws, stream);
+    if (e == cudaErrorInvalidConfiguration) return fail(PHB_ERR_SHAPE, "shape does not fit the attention kernels");
+    if (e != cudaSuccess) return cuda_fail(e, "attention launch");
     return ok();
 }
 

@@ -147,11 +147,19 @@ cudaError_t read_dev_err_moe(int* code);
 cudaError_t read_dev_err_prefill(int* code);
 cudaError_t read_dev_err_decode_persistent(int* code);
 cudaError_t read_dev_err_gemv_rows(int* code);
+cudaError_t read_dev_err_attention(int* code);
 
 // Row-resident batched GEMV (gemv_rows.cu): plain store, batch 2..8,
 // K % 256 == 0. ksplit_out receives the K splits (> 1: partials in q.ws
 // still need splitk reduction).
 size_t gemv_rows_ws_floats(int qt, int64_t n, int64_t k, int batch);
 cudaError_t gemv_rows_run(const GemvReq& q, cudaStream_t s, int* ksplit_out);
+
+// ---------------------------------------------------------------- decode attention
+// Split-KV attention of one token over an fp16 cache (attention.cu).
+bool attention_shape_ok(int n_q, int n_kv, int hd);
+size_t attention_ws_bytes(int n_q, int n_kv, int hd, int64_t len);
+cudaError_t attention_run(const float* q, const void* k, const void* v, float* out, int n_q, int n_kv, int hd,
+                          int64_t len, float scale, void* ws, cudaStream_t s);
 
 }  // namespace phb

@@ -30,7 +30,7 @@ def declared_functions():
 def test_header_declares_the_expected_calls():
     names = declared_functions()
     for want in ["phb_dequant_q8_0", "phb_dequant_q4_k", "phb_gemv_q8_0", "phb_gemv_q4_k", "phb_ffn_swiglu",
-                 "phb_moe_ffn", "phb_gemm_q_prefill", "phb_decode_step", "phb_last_error"]:
+                 "phb_moe_ffn", "phb_gemm_q_prefill", "phb_decode_step", "phb_attention_decode", "phb_last_error"]:
         assert want in names
 
 
@@ -110,3 +110,20 @@ def test_prefill_and_decode_reject_bad_arguments(lib):
     assert d(8, ctypes.cast(bad, ctypes.c_void_p), 1, 2048, 16, 4, 128, 5632, FAKE, FAKE + 256, FAKE, 1 << 30,
              None) == INVALID
     assert d(8, lp, 1, 2048, 16, 4, 128, 5632, FAKE, FAKE + 256, FAKE, 64, None) == WORKSPACE
+
+
+def test_attention_rejects_bad_arguments(lib):
+    a = lib.phb_attention_decode
+    ptrs = [FAKE, FAKE, FAKE, FAKE]
+    assert a(*ptrs, 4096, 16, 4, 96, 0.1, FAKE, 1 << 30, None) == SHAPE and "head_dim" in _err(lib)
+    assert a(*ptrs, 4096, 6, 4, 128, 0.1, FAKE, 1 << 30, None) == SHAPE
+    assert a(*ptrs, 0, 16, 4, 128, 0.1, FAKE, 1 << 30, None) == INVALID
+    assert a(*ptrs, (1 << 26) + 1, 16, 4, 128, 0.1, FAKE, 1 << 30, None) == INVALID
+    assert a(None, FAKE, FAKE, FAKE, 4096, 16, 4, 128, 0.1, FAKE, 1 << 30, None) == INVALID
+    assert a(FAKE, FAKE + 8, FAKE, FAKE, 4096, 16, 4, 128, 0.1, FAKE, 1 << 30, None) == ALIGN
+    assert a(*ptrs, 4096, 16, 4, 128, float("inf"), FAKE, 1 << 30, None) == INVALID
+    assert a(*ptrs, 4096, 16, 4, 128, 0.1, FAKE, 16, None) == WORKSPACE
+    assert lib.phb_attention_decode_workspace_size(4096, 16, 4, 128) > 0
+    assert lib.phb_attention_decode_workspace_size(4096, 16, 4, 80) == 0
+    assert lib.phb_attention_decode_workspace_size(0, 16, 4, 128) == 0
+    assert lib.phb_attention_decode_workspace_size(4096, 16, 5, 128) == 0
