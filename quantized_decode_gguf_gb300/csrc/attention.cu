@@ -21,6 +21,8 @@
 //     argument, so these loops unroll).
 //  2. attn_merge_kernel, one CTA per query head: out = sum_c e^(m_c - M) o_c /
 //     sum_c e^(m_c - M) l_c over the chunks c in order (M their maximum).
+// Scores and maxima are held in base 2 (scale folded with log2 e), so every
+// exponential is one exp2f.
 // Every order is fixed, so repeated calls give identical bits. K and V are
 // each read once from HBM (query-head groups beyond 8 re-read them from L2).
 #include <cuda.h>
@@ -59,7 +61,7 @@ constexpr int kNC = 32 * kCW;
 constexpr int kThreads = kNC + 32;    // + one producer warp
 constexpr int kMaxHeads = 8;          // query heads per CTA
 constexpr int kMaxStages = 8;
-constexpr int kWarpFloats = 48;       // per consumer warp: p [4][8], alpha [8], spare [8]
+constexpr int kWarpFloats = 80;       // per consumer warp: (p, p) pairs [4][8], alpha [8], spare [8]
 
 struct AttnParams {
     const float* q;
@@ -67,7 +69,7 @@ struct AttnParams {
     float* ml_part;  // [nsplit][n_q][2]: chunk maximum and exp-sum
     int64_t len;
     int n_q, n_kv, group, hgroups, chunk, ns;
-    float scale;
+    float scale;     // the caller's scale times log2(e)
     uint32_t stage_bytes, q_off, warp_off, bar_off;
 };
 
@@ -157,9 +159,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             const uint64_t pol = policy_evict_first();
             constexpr uint32_t kRowBytes = 2 * HD;
             int issued = 0;
-            for (int t = 0; t < ntiles; ++t) {
-                const int slot = t % p.ns;
-                if (t >= p.ns && !mbar_wait(&empty[slot], ((t / p.ns) - 1) & 1, &g_attn_err)) break;
+            for (int t = 0, slot = 0, phase = 0; t < ntiles; ++t) {
+                if (t >= p.ns && !mbar_wait(&empty[slot], phase ^ 1, &g_attn_err)) break;
                 // a box past n_ctx is zero-filled and still counts its full size
                 mbar_arrive_expect_tx(&full[slot], 2 * kTileRows * kRowBytes);
                 uint8_t* st = smem + static_cast<size_t>(slot) * p.stage_bytes;
@@ -167,6 +168,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                 tma_load_3d(st, &tmap_k, 0, kv, y0, &full[slot], pol);
                 tma_load_3d(st + kTileRows * kRowBytes, &tmap_v, 0, kv, y0, &full[slot], pol);
                 ++issued;
+                if (++slot == p.ns) {
+                    slot = 0;
+                    phase ^= 1;
+                }
             }
             // copies still in flight land before the CTA may exit (bounded; long done on the normal path)
             for (int t = max(0, issued - p.ns); t < issued; ++t)
@@ -181,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // head, so a quarter-warp reads 128 contiguous bytes and each K element is
     // converted once.
     const int jl = lane >> 3, u = lane & 7;
-    float qr[kQReg ? GP : 1][kQReg ? CPL : 1][8];
+    float2 qr[kQReg ? GP : 1][kQReg ? CPL : 1][4];  // pairs, as the packed FMA takes them
     float* qsm = reinterpret_cast<float*>(smem + p.q_off);  // [GP][2][NCH][4]: chunk halves, chunk-major
     if constexpr (kQReg) {
 #pragma unroll
@@ -189,8 +194,10 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int i = 0; i < CPL; ++i)
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    qr[h][i][e] = h < gh ? p.q[static_cast<int64_t>(h0 + h) * HD + (u + 8 * i) * 8 + e] : 0.f;
+                for (int e = 0; e < 4; ++e) {
+                    const float* src = p.q + static_cast<int64_t>(h0 + h) * HD + (u + 8 * i) * 8 + 2 * e;
+                    qr[h][i][e] = h < gh ? make_float2(src[0], src[1]) : make_float2(0.f, 0.f);
+                }
     } else {
         for (int i = tid; i < GP * HD; i += kNC) {
             const int h = i / HD, d = i - h * HD, c = d >> 3, e = d & 7;
@@ -199,8 +206,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         named_sync<kNC>();
     }
 
-    float* pw = reinterpret_cast<float*>(smem + p.warp_off) + warp * kWarpFloats;  // p [4 positions][8 heads]
-    float* aw = pw + 32;                                                          // alpha [8 heads]
+    float2* pw = reinterpret_cast<float2*>(smem + p.warp_off) + warp * (kWarpFloats / 2);  // (p, p) [4 pos][8 heads]
+    float* aw = reinterpret_cast<float*>(pw + 32);                                         // alpha [8 heads]
     float m_run = -INFINITY, l_run = 0.f;  // of head hl, below
     int hl = 0;
     float2 acc[GP][E / 2];
@@ -209,9 +216,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int e = 0; e < E / 2; ++e) acc[h][e] = make_float2(0.f, 0.f);
 
-    for (int t = 0; t < ntiles; ++t) {
-        const int slot = t % p.ns;
-        if (!mbar_wait_warp(&full[slot], (t / p.ns) & 1, &g_attn_err)) break;
+    for (int t = 0, slot = 0, phase = 0; t < ntiles; ++t) {
+        if (!mbar_wait_warp(&full[slot], phase, &g_attn_err)) break;
         const uint8_t* st = smem + static_cast<size_t>(slot) * p.stage_bytes;
         const int rows = min(kTileRows, np - t * kTileRows);
 
@@ -228,18 +234,24 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const float2 k0 = h2f(raw.x), k1 = h2f(raw.y), k2 = h2f(raw.z), k3 = h2f(raw.w);
 #pragma unroll
                 for (int h = 0; h < GP; ++h) {
-                    float4 qa, qb;
+                    float2 q0, q1, q2, q3;
                     if constexpr (kQReg) {
-                        qa = make_float4(qr[h][i][0], qr[h][i][1], qr[h][i][2], qr[h][i][3]);
-                        qb = make_float4(qr[h][i][4], qr[h][i][5], qr[h][i][6], qr[h][i][7]);
+                        q0 = qr[h][i][0];
+                        q1 = qr[h][i][1];
+                        q2 = qr[h][i][2];
+                        q3 = qr[h][i][3];
                     } else {
-                        qa = *reinterpret_cast<const float4*>(qsm + ((h * 2) * NCH + u + 8 * i) * 4);
-                        qb = *reinterpret_cast<const float4*>(qsm + ((h * 2 + 1) * NCH + u + 8 * i) * 4);
+                        const float4 qa = *reinterpret_cast<const float4*>(qsm + ((h * 2) * NCH + u + 8 * i) * 4);
+                        const float4 qb = *reinterpret_cast<const float4*>(qsm + ((h * 2 + 1) * NCH + u + 8 * i) * 4);
+                        q0 = make_float2(qa.x, qa.y);
+                        q1 = make_float2(qa.z, qa.w);
+                        q2 = make_float2(qb.x, qb.y);
+                        q3 = make_float2(qb.z, qb.w);
                     }
-                    a2[h] = __ffma2_rn(make_float2(qa.x, qa.y), k0, a2[h]);
-                    a2[h] = __ffma2_rn(make_float2(qa.z, qa.w), k1, a2[h]);
-                    a2[h] = __ffma2_rn(make_float2(qb.x, qb.y), k2, a2[h]);
-                    a2[h] = __ffma2_rn(make_float2(qb.z, qb.w), k3, a2[h]);
+                    a2[h] = __ffma2_rn(q0, k0, a2[h]);
+                    a2[h] = __ffma2_rn(q1, k1, a2[h]);
+                    a2[h] = __ffma2_rn(q2, k2, a2[h]);
+                    a2[h] = __ffma2_rn(q3, k3, a2[h]);
                 }
             }
         }
@@ -254,13 +266,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         float mt = fmaxf(s, __shfl_xor_sync(0xFFFFFFFFu, s, 8));
         mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, 16));
         const float m_new = fmaxf(m_run, mt);
-        const float alpha = m_new == -INFINITY ? 1.f : expf(m_run - m_new);
-        const float pj = s == -INFINITY ? 0.f : expf(s - m_new);
+        const float alpha = m_new == -INFINITY ? 1.f : exp2f(m_run - m_new);
+        const float pj = s == -INFINITY ? 0.f : exp2f(s - m_new);
         float ls = pj + __shfl_xor_sync(0xFFFFFFFFu, pj, 8);
         ls += __shfl_xor_sync(0xFFFFFFFFu, ls, 16);
         l_run = fmaf(l_run, alpha, ls);
         m_run = m_new;
-        pw[jl * 8 + hl] = pj;
+        pw[jl * 8 + hl] = make_float2(pj, pj);
         if (jl == 0) aw[hl] = alpha;
         const bool rescale = __any_sync(0xFFFFFFFFu, alpha != 1.f);
         __syncwarp();
@@ -294,29 +306,29 @@ __global__ void __launch_bounds__(kThreads, 2)
                     vv[2] = h2f(w.z);
                     vv[3] = h2f(w.w);
                 }
-                float ph[GP];
-                if constexpr (GP >= 4) {
+                float2 ph[GP];
+                if constexpr (GP >= 2) {
 #pragma unroll
-                    for (int h = 0; h < GP; h += 4) {
+                    for (int h = 0; h < GP; h += 2) {
                         const float4 p4 = *reinterpret_cast<const float4*>(pw + r * 8 + h);
-                        ph[h] = p4.x;
-                        ph[h + 1] = p4.y;
-                        ph[h + 2] = p4.z;
-                        ph[h + 3] = p4.w;
+                        ph[h] = make_float2(p4.x, p4.y);
+                        ph[h + 1] = make_float2(p4.z, p4.w);
                     }
                 } else {
-#pragma unroll
-                    for (int h = 0; h < GP; ++h) ph[h] = pw[r * 8 + h];
+                    ph[0] = pw[r * 8];
                 }
 #pragma unroll
                 for (int h = 0; h < GP; ++h)
 #pragma unroll
-                    for (int e = 0; e < E / 2; ++e)
-                        acc[h][e] = __ffma2_rn(make_float2(ph[h], ph[h]), vv[e], acc[h][e]);
+                    for (int e = 0; e < E / 2; ++e) acc[h][e] = __ffma2_rn(ph[h], vv[e], acc[h][e]);
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
+        if (++slot == p.ns) {
+            slot = 0;
+            phase ^= 1;
+        }
     }
 
     // ---------------- combine the warps' states, in warp order
@@ -334,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             float mx = -INFINITY;
             for (int w = 0; w < kCW; ++w) mx = fmaxf(mx, wml[(w * kMaxHeads + h) * 2]);
             const float mw = wml[(warp * kMaxHeads + h) * 2];
-            const float f = mw == -INFINITY ? 0.f : expf(mw - mx);
+            const float f = mw == -INFINITY ? 0.f : exp2f(mw - mx);
             float* dst = red + (warp * gh + h) * HD + lane * E;
 #pragma unroll
             for (int e = 0; e < E / 2; ++e) {
@@ -356,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         float l = 0.f;
         for (int w = 0; w < kCW; ++w) {
             const float mw = wml[(w * kMaxHeads + tid) * 2];
-            const float f = mw == -INFINITY ? 0.f : expf(mw - mx);
+            const float f = mw == -INFINITY ? 0.f : exp2f(mw - mx);
             l = fmaf(f, wml[(w * kMaxHeads + tid) * 2 + 1], l);
         }
         float* ml = p.ml_part + (static_cast<int64_t>(split) * p.n_q + h0 + tid) * 2;
@@ -365,23 +377,63 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 }
 
-// One CTA per query head, one thread per output element.
-__global__ void __launch_bounds__(256) attn_merge_kernel(const float* __restrict__ o_part,
-                                                         const float* __restrict__ ml_part, float* __restrict__ out,
-                                                         int n_q, int hd, int nsplit) {
+// One CTA of 256 threads per query head. The chunk weights w_c = 2^(m_c - M)
+// and the exp-sums l_c go to shared memory in parallel; thread (d, part)
+// sums w_c o_c[d] over the chunks c = part, part + parts, ... (loads unrolled,
+// so they overlap), and the parts and l are added in a fixed order.
+constexpr int kMergeThreads = 256;
+
+__global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const float* __restrict__ o_part,
+                                                                   const float* __restrict__ ml_part,
+                                                                   float* __restrict__ out, int n_q, int hd,
+                                                                   int nsplit) {
+    extern __shared__ float msm[];  // w [nsplit] | l [nsplit] | partial sums [256] | warp maxima [8]
+    float* w = msm;
+    float* lc = w + nsplit;
+    float* part_sum = lc + nsplit;
+    float* wmax = part_sum + kMergeThreads;
     pdl_launch_dependents();
     pdl_wait();
-    const int h = blockIdx.x, d = threadIdx.x;
+    const int h = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     float mx = -INFINITY;
-    for (int c = 0; c < nsplit; ++c) mx = fmaxf(mx, ml_part[(static_cast<int64_t>(c) * n_q + h) * 2]);
-    float l = 0.f, acc = 0.f;
-    for (int c = 0; c < nsplit; ++c) {
-        const float* ml = ml_part + (static_cast<int64_t>(c) * n_q + h) * 2;
-        const float f = expf(ml[0] - mx);
-        l = fmaf(f, ml[1], l);
-        acc = fmaf(f, o_part[(static_cast<int64_t>(c) * n_q + h) * hd + d], acc);
+    for (int c = tid; c < nsplit; c += kMergeThreads) {
+        const float2 ml = *reinterpret_cast<const float2*>(ml_part + (static_cast<int64_t>(c) * n_q + h) * 2);
+        w[c] = ml.x;
+        lc[c] = ml.y;
+        mx = fmaxf(mx, ml.x);
     }
-    out[static_cast<int64_t>(h) * hd + d] = acc / l;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    if (lane == 0) wmax[warp] = mx;
+    __syncthreads();
+    mx = wmax[0];
+#pragma unroll
+    for (int i = 1; i < kMergeThreads / 32; ++i) mx = fmaxf(mx, wmax[i]);
+    for (int c = tid; c < nsplit; c += kMergeThreads) w[c] = exp2f(w[c] - mx);
+    __syncthreads();
+    const int parts = kMergeThreads / hd;  // hd divides 256
+    const int d = tid % hd, pt = tid / hd;
+    const float* src = o_part + static_cast<int64_t>(h) * hd + d;
+    const int64_t cstride = static_cast<int64_t>(n_q) * hd;
+    float acc = 0.f;
+    int c = pt;
+    for (; c + 7 * parts < nsplit; c += 8 * parts) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = src[(c + u * parts) * cstride];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) acc = fmaf(w[c + u * parts], v[u], acc);
+    }
+    for (; c < nsplit; c += parts) acc = fmaf(w[c], src[c * cstride], acc);
+    part_sum[tid] = acc;
+    __syncthreads();
+    if (pt == 0) {
+        float sum = part_sum[d];
+        for (int q = 1; q < parts; ++q) sum += part_sum[q * hd + d];
+        float l = 0.f;
+        for (int k = 0; k < nsplit; ++k) l = fmaf(w[k], lc[k], l);
+        out[static_cast<int64_t>(h) * hd + d] = sum / l;
+    }
 }
 
 struct AttnPlan {
@@ -498,7 +550,8 @@ cudaError_t attention_run(const float* q, const void* k, const void* v, float* o
     p.hgroups = pl.hgroups;
     p.chunk = pl.chunk;
     p.ns = pl.ns;
-    p.scale = scale;
+    // scores are kept in base 2: s2 = scale * log2(e) * q.k, so exp(s - m) = 2^(s2 - m2)
+    p.scale = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     p.stage_bytes = pl.stage_bytes;
     p.q_off = pl.q_off;
     p.warp_off = pl.warp_off;
@@ -510,9 +563,10 @@ cudaError_t attention_run(const float* q, const void* k, const void* v, float* o
                     : hd == 128 ? launch_split_e<4>(gp, pl, grid, maps, p, s)
                                 : launch_split_e<8>(gp, pl, grid, maps, p, s);
     if (e != cudaSuccess) return e;
-    return launch_kernel(attn_merge_kernel, dim3(static_cast<unsigned>(n_q)), dim3(static_cast<unsigned>(hd)), 0, s,
-                         true, static_cast<const float*>(p.o_part), static_cast<const float*>(p.ml_part), out, n_q,
-                         hd, pl.nsplit);
+    const size_t msmem = (2 * static_cast<size_t>(pl.nsplit) + kMergeThreads + 8) * sizeof(float);
+    return launch_kernel(attn_merge_kernel, dim3(static_cast<unsigned>(n_q)), dim3(kMergeThreads), msmem, s, true,
+                         static_cast<const float*>(p.o_part), static_cast<const float*>(p.ml_part), out, n_q, hd,
+                         pl.nsplit);
 }
 
 }  // namespace phb
