@@ -436,24 +436,414 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const float* 
     }
 }
 
+// ---------------------------------------------------------------- tensor-core score path (head_dim 64, 128)
+// The scores of a 128-position stage are one tcgen05 MMA chain:
+//   S^T [128 positions][16] = K [128][head_dim] . B^T,
+// with B's 16 rows the CTA's (up to) 8 query heads split into fp16 high and
+// low parts (rows h and 8 + h). Each head's query is first scaled by a power
+// of two 2^e_h that brings its largest magnitude into [2^14, 2^15), so
+// q 2^e_h = hi + lo to about 2^-22 relative (the scaling is exact and is
+// undone with the score scale). K is fp16 and enters the MMA unconverted;
+// products are exact and summed in fp32. Two warpgroups of 4 consumer warps
+// take alternate stages: each warp reads its 32 positions' scores from TMEM
+// (one thread per position, all heads in registers), keeps a per-warp
+// online softmax, and accumulates the value rows on the CUDA cores as the
+// other kernel does. The accumulator has two 16-column TMEM buffers, so the
+// MMA of stage t + 1 runs while stage t is consumed.
+constexpr int kTcRows = 128;                   // positions per stage (MMA M)
+constexpr int kTcCW = 8;                       // consumer warps
+constexpr int kTcTmaWarp = kTcCW;
+constexpr int kTcMmaWarp = kTcCW + 1;
+constexpr int kTcThreads = 32 * (kTcCW + 2);
+constexpr uint32_t kTcTmemCols = 32;           // two 16-column score buffers
+constexpr int kTcMaxStages = 6;
+constexpr uint32_t kTcKBlock = kTcRows * 128;  // one 64-dim block of a K stage, 128-byte swizzled rows
+constexpr uint32_t kTcQBlock = 16 * 128;       // one 64-dim block of the 16 query rows
+// kind::f16: D fp32, A and B fp16, both K-major, N = 16, M = 128
+constexpr uint32_t kTcIdesc = (1u << 4) | (uint32_t(16 >> 3) << 17) | (uint32_t(kTcRows >> 4) << 24);
+
+struct TcParams {
+    const float* q;
+    float* o_part;
+    float* ml_part;
+    int64_t len;
+    int n_q, n_kv, group, hgroups, chunk, ns;
+    float scale;  // the caller's scale times log2(e)
+    uint32_t stage_bytes, qb_off, pbuf_off, warp_off, bar_off;
+};
+
+__device__ __forceinline__ uint64_t desc_sw128(const void* ptr) {
+    // K-major operand in the 128-byte swizzle layout: 8-row groups of
+    // 128-byte rows, 1024 bytes apart (stride byte offset); version 1.
+    const uint64_t addr = smem_addr(ptr);
+    return ((addr & 0x3FFFFull) >> 4) | (1ull << 16) | ((1024ull >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+__device__ __forceinline__ void tc_mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(kTcIdesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+
+// 16 consecutive TMEM columns of this warp's 32 lanes, one lane per thread.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ uint32_t pack_half2(__half a, __half b) {
+    return static_cast<uint32_t>(__half_as_ushort(a)) | (static_cast<uint32_t>(__half_as_ushort(b)) << 16);
+}
+
+// Shared memory (1024-byte aligned base): ring [ns][K blocks | V rows] |
+// query operand [HD/64][16 rows][128 B] | per-warp (p, p) [8][32 pos][8 heads]
+// | per-warp (m, l) [8][8][2], head scales [8] | mbarriers, TMEM address.
+template <int GP, int HD>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                   const __grid_constant__ TcParams p) {
+    constexpr int E = HD / 32;
+    constexpr int KB = HD / 64;
+    constexpr uint32_t kVOff = KB * kTcKBlock;
+    extern __shared__ uint8_t tc_smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t{1023});
+    uint8_t* qb = smem + p.qb_off;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
+    uint64_t* empty = full + kTcMaxStages;
+    uint64_t* sfull = empty + kTcMaxStages;
+    uint64_t* sfree = sfull + 2;
+    uint64_t* qready = sfree + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qready + 1);
+    float* wml = reinterpret_cast<float*>(smem + p.warp_off);  // [warp][8 heads][m, l]
+    float* hscale = wml + kTcCW * kMaxHeads * 2;              // [8]
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int kv = blockIdx.x / p.hgroups, hg = blockIdx.x - kv * p.hgroups;
+    const int h0 = kv * p.group + hg * kMaxHeads;
+    const int gh = min(kMaxHeads, p.group - hg * kMaxHeads);
+    const int split = blockIdx.y;
+    const int64_t pos0 = static_cast<int64_t>(split) * p.chunk;
+    const int np = static_cast<int>(min(static_cast<int64_t>(p.chunk), p.len - pos0));
+    const int ntiles = (np + kTcRows - 1) / kTcRows;
+
+    if (tid == 0) {
+        for (int s = 0; s < p.ns; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 4);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sfull[b], 1);
+            mbar_init(&sfree[b], 4);
+        }
+        mbar_init(qready, kTcCW);
+        fence_barrier_init();
+    }
+    if (warp == kTcMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                     "r"(kTcTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_before();
+    __syncthreads();
+    tc_after();
+    const uint32_t tmem = *tmem_slot;
+    pdl_launch_dependents();
+    pdl_wait();  // the query and the cache may come from the kernels before this one
+
+    if (warp == kTcTmaWarp) {
+        // ---------------- producer: per stage hd/64 swizzled K boxes and one V box
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            int issued = 0;
+            for (int t = 0, slot = 0, phase = 0; t < ntiles; ++t) {
+                if (t >= p.ns && !mbar_wait(&empty[slot], phase ^ 1, &g_attn_err)) break;
+                // boxes past n_ctx are zero-filled and still count their full size
+                mbar_arrive_expect_tx(&full[slot], kVOff + kTcRows * HD * 2);
+                uint8_t* st = smem + static_cast<size_t>(slot) * p.stage_bytes;
+                const int y0 = static_cast<int>(pos0) + t * kTcRows;
+#pragma unroll
+                for (int c = 0; c < KB; ++c) tma_load_3d(st + c * kTcKBlock, &tmap_k, 64 * c, kv, y0, &full[slot], pol);
+                tma_load_3d(st + kVOff, &tmap_v, 0, kv, y0, &full[slot], pol);
+                ++issued;
+                if (++slot == p.ns) {
+                    slot = 0;
+                    phase ^= 1;
+                }
+            }
+            for (int t = max(0, issued - p.ns); t < issued; ++t)
+                mbar_wait(&full[t % p.ns], (t / p.ns) & 1, &g_attn_err);
+        }
+    } else if (warp == kTcMmaWarp) {
+        // ---------------- one thread issues the score MMAs
+        if (lane == 0) {
+            int issued = 0;
+            if (mbar_wait(qready, 0, &g_attn_err)) {
+                for (int t = 0, slot = 0, phase = 0; t < ntiles; ++t) {
+                    const int b = t & 1;
+                    if (!mbar_wait(&full[slot], phase, &g_attn_err)) break;
+                    if (t >= 2 && !mbar_wait(&sfree[b], ((t >> 1) - 1) & 1, &g_attn_err)) break;
+                    tc_after();
+                    const uint8_t* st = smem + static_cast<size_t>(slot) * p.stage_bytes;
+#pragma unroll
+                    for (int c = 0; c < KB; ++c)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            tc_mma_f16(tmem + 16 * b, desc_sw128(st + c * kTcKBlock + kk * 32),
+                                       desc_sw128(qb + c * kTcQBlock + kk * 32), (c | kk) ? 1u : 0u);
+                    tc_commit(&sfull[b]);
+                    ++issued;
+                    if (++slot == p.ns) {
+                        slot = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            // every MMA issued has completed before TMEM is released (bounded; long done on the normal path)
+            for (int t = max(0, issued - 2); t < issued; ++t) mbar_wait(&sfull[t & 1], (t >> 1) & 1, &g_attn_err);
+        }
+    } else {
+        // ---------------- consumers
+        // query operand: warp w writes rows w (high part) and 8 + w (low part)
+        {
+            const int h = warp;
+            float qv[E];
+            float mx = 0.f;
+#pragma unroll
+            for (int i = 0; i < E; ++i) {
+                qv[i] = h < gh ? p.q[static_cast<int64_t>(h0 + h) * HD + E * lane + i] : 0.f;
+                mx = fmaxf(mx, fabsf(qv[i]));
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+            int ex = 0;
+            frexpf(mx, &ex);
+            const int e = mx > 0.f ? 15 - ex : 0;
+            if (lane == 0) hscale[h] = ldexpf(p.scale, -e);
+            __half hi[E], lo[E];
+#pragma unroll
+            for (int i = 0; i < E; ++i) {
+                const float qs = ldexpf(qv[i], e);
+                hi[i] = __float2half_rn(qs);
+                lo[i] = __float2half_rn(qs - __half2float(hi[i]));
+            }
+            const int d0 = E * lane, blk = d0 >> 6, ch = (d0 & 63) >> 3, byte = (d0 & 7) * 2;
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+                const int r = h + 8 * part;
+                uint8_t* dst = qb + blk * kTcQBlock + r * 128 + ((ch ^ (r & 7)) << 4) + byte;
+                const __half* src = part == 0 ? hi : lo;
+                if constexpr (E == 2) {
+                    *reinterpret_cast<uint32_t*>(dst) = pack_half2(src[0], src[1]);
+                } else {
+                    *reinterpret_cast<uint2*>(dst) = make_uint2(pack_half2(src[0], src[1]), pack_half2(src[2], src[3]));
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(qready);
+        }
+        named_sync<32 * kTcCW>();  // head scales visible to every consumer
+
+        const int g = warp >> 2, wq = warp & 3;
+        float2* pb = reinterpret_cast<float2*>(smem + p.pbuf_off) + warp * (32 * kMaxHeads);  // (p, p) [32][8]
+        float hs[GP];
+#pragma unroll
+        for (int h = 0; h < GP; ++h) hs[h] = hscale[h];
+        float m_run[GP], l_lane[GP];
+        float2 acc[GP][E / 2];
+#pragma unroll
+        for (int h = 0; h < GP; ++h) {
+            m_run[h] = -INFINITY;
+            l_lane[h] = 0.f;
+#pragma unroll
+            for (int e = 0; e < E / 2; ++e) acc[h][e] = make_float2(0.f, 0.f);
+        }
+        for (int t = g; t < ntiles; t += 2) {
+            const int slot = t % p.ns, b = t & 1;
+            if (!mbar_wait_warp(&sfull[b], (t >> 1) & 1, &g_attn_err)) break;
+            tc_after();
+            __syncwarp();  // the TMEM load is warp-collective
+            float sv[16];
+            tmem_ld16(tmem + (static_cast<uint32_t>(32 * wq) << 16) + 16 * b, sv);
+            tc_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sfree[b]);
+            const int rows = min(kTcRows, np - t * kTcRows);
+            const bool valid = 32 * wq + lane < rows;
+            bool moved = false;
+            float alpha[GP];
+#pragma unroll
+            for (int h = 0; h < GP; ++h) {
+                const float s = (valid && h < gh) ? (sv[h] + sv[8 + h]) * hs[h] : -INFINITY;
+                float mt = s;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, o));
+                const float m_new = fmaxf(m_run[h], mt);
+                alpha[h] = m_new == -INFINITY ? 1.f : exp2f(m_run[h] - m_new);
+                const float pj = s == -INFINITY ? 0.f : exp2f(s - m_new);
+                l_lane[h] = fmaf(l_lane[h], alpha[h], pj);
+                m_run[h] = m_new;
+                moved |= alpha[h] != 1.f;
+                pb[lane * kMaxHeads + h] = make_float2(pj, pj);
+            }
+            __syncwarp();
+            if (moved) {  // uniform over the warp: the maxima are
+#pragma unroll
+                for (int h = 0; h < GP; ++h)
+#pragma unroll
+                    for (int e = 0; e < E / 2; ++e)
+                        acc[h][e] = make_float2(acc[h][e].x * alpha[h], acc[h][e].y * alpha[h]);
+            }
+            // value rows of this warp's 32 positions (the stage's copies have landed: observe it)
+            if (!mbar_wait_warp(&full[slot], (t / p.ns) & 1, &g_attn_err)) break;
+            const uint8_t* vb = smem + static_cast<size_t>(slot) * p.stage_bytes + kVOff +
+                                static_cast<size_t>(32 * wq) * (2 * HD) + lane * (2 * E);
+            const int nrow = min(32, rows - 32 * wq);
+            for (int r = 0; r < nrow; ++r) {
+                const uint8_t* vr = vb + r * (2 * HD);
+                float2 vv[E / 2];
+                if constexpr (E == 2) {
+                    vv[0] = h2f(*reinterpret_cast<const uint32_t*>(vr));
+                } else {
+                    const uint2 w = *reinterpret_cast<const uint2*>(vr);
+                    vv[0] = h2f(w.x);
+                    vv[1] = h2f(w.y);
+                }
+                float2 ph[GP];
+                if constexpr (GP >= 2) {
+#pragma unroll
+                    for (int h = 0; h < GP; h += 2) {
+                        const float4 p4 = *reinterpret_cast<const float4*>(pb + r * kMaxHeads + h);
+                        ph[h] = make_float2(p4.x, p4.y);
+                        ph[h + 1] = make_float2(p4.z, p4.w);
+                    }
+                } else {
+                    ph[0] = pb[r * kMaxHeads];
+                }
+#pragma unroll
+                for (int h = 0; h < GP; ++h)
+#pragma unroll
+                    for (int e = 0; e < E / 2; ++e) acc[h][e] = __ffma2_rn(ph[h], vv[e], acc[h][e]);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+        }
+
+        // ---------------- combine the 8 warps' states, in warp order
+#pragma unroll
+        for (int h = 0; h < GP; ++h)
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) l_lane[h] += __shfl_xor_sync(0xFFFFFFFFu, l_lane[h], o);
+        if (lane == 0) {
+#pragma unroll
+            for (int h = 0; h < GP; ++h) {
+                wml[(warp * kMaxHeads + h) * 2] = m_run[h];
+                wml[(warp * kMaxHeads + h) * 2 + 1] = l_lane[h];
+            }
+        }
+        named_sync<32 * kTcCW>();  // every stage consumed: the ring now holds the warps' scaled outputs
+        float* red = reinterpret_cast<float*>(smem);  // [warp][gh][HD]
+#pragma unroll
+        for (int h = 0; h < GP; ++h) {
+            if (h < gh) {
+                float mx = -INFINITY;
+                for (int w = 0; w < kTcCW; ++w) mx = fmaxf(mx, wml[(w * kMaxHeads + h) * 2]);
+                const float mw = wml[(warp * kMaxHeads + h) * 2];
+                const float f = mw == -INFINITY ? 0.f : exp2f(mw - mx);
+                float* dst = red + (warp * gh + h) * HD + lane * E;
+#pragma unroll
+                for (int e = 0; e < E / 2; ++e) {
+                    dst[2 * e] = f * acc[h][e].x;
+                    dst[2 * e + 1] = f * acc[h][e].y;
+                }
+            }
+        }
+        named_sync<32 * kTcCW>();
+        const int64_t obase = (static_cast<int64_t>(split) * p.n_q + h0) * HD;
+        for (int i = tid; i < gh * HD; i += 32 * kTcCW) {
+            float sum = 0.f;
+            for (int w = 0; w < kTcCW; ++w) sum += red[w * gh * HD + i];
+            p.o_part[obase + i] = sum;
+        }
+        if (tid < gh) {
+            float mx = -INFINITY;
+            for (int w = 0; w < kTcCW; ++w) mx = fmaxf(mx, wml[(w * kMaxHeads + tid) * 2]);
+            float l = 0.f;
+            for (int w = 0; w < kTcCW; ++w) {
+                const float mw = wml[(w * kMaxHeads + tid) * 2];
+                const float f = mw == -INFINITY ? 0.f : exp2f(mw - mx);
+                l = fmaf(f, wml[(w * kMaxHeads + tid) * 2 + 1], l);
+            }
+            float* ml = p.ml_part + (static_cast<int64_t>(split) * p.n_q + h0 + tid) * 2;
+            ml[0] = mx;
+            ml[1] = l;
+        }
+    }
+    tc_before();
+    __syncthreads();
+    if (warp == kTcMmaWarp) {
+        __syncwarp();
+        tc_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcTmemCols) : "memory");
+    }
+}
+
 struct AttnPlan {
+    bool tc = false;  // tensor-core score kernel (head_dim 64, 128) or the CUDA-core one (256)
     int hgroups = 1, chunk = 0, nsplit = 0, ns = 0;
-    uint32_t stage_bytes = 0, q_off = 0, warp_off = 0, bar_off = 0;
+    uint32_t stage_bytes = 0, q_off = 0, warp_off = 0, bar_off = 0, pbuf_off = 0;
     size_t smem = 0;
 };
 
-
 AttnPlan plan_attn(int n_q, int n_kv, int hd, int64_t len) {
     AttnPlan pl;
+    pl.tc = hd <= 128;
     const int group = n_q / n_kv;
     pl.hgroups = (group + kMaxHeads - 1) / kMaxHeads;
-    const int ctas = 2;  // CTAs per SM
+    const int ctas = pl.tc ? 1 : 2;  // CTAs per SM
+    const int rows = pl.tc ? kTcRows : kTileRows;
     const int64_t items = static_cast<int64_t>(n_kv) * pl.hgroups;
     const int64_t want = std::max<int64_t>(1, (static_cast<int64_t>(ctas) * device_sm_count() + items - 1) / items);
     int64_t chunk = (len + want - 1) / want;
-    chunk = (chunk + kTileRows - 1) / kTileRows * kTileRows;
+    chunk = (chunk + rows - 1) / rows * rows;
     pl.chunk = static_cast<int>(chunk);
     pl.nsplit = static_cast<int>((len + chunk - 1) / chunk);
+    if (pl.tc) {
+        // ring of 128-position stages | query operand | (p, p) buffers | warp states | barriers
+        pl.stage_bytes = static_cast<uint32_t>((hd / 64) * kTcKBlock + kTcRows * hd * 2);
+        const size_t qb_bytes = static_cast<size_t>(hd / 64) * kTcQBlock;
+        const size_t pbuf_bytes = static_cast<size_t>(kTcCW) * 32 * kMaxHeads * sizeof(float2);
+        const size_t warp_bytes = 1024;  // (m, l) [8][8][2] and head scales [8]
+        const size_t bar_bytes = 256;
+        const size_t fixed = qb_bytes + pbuf_bytes + warp_bytes + bar_bytes;
+        pl.ns = static_cast<int>(std::min<size_t>(kTcMaxStages, (kSmemOptin - 1024 - fixed) / pl.stage_bytes));
+        pl.q_off = static_cast<uint32_t>(static_cast<size_t>(pl.ns) * pl.stage_bytes);
+        pl.pbuf_off = static_cast<uint32_t>(pl.q_off + qb_bytes);
+        pl.warp_off = static_cast<uint32_t>(pl.pbuf_off + pbuf_bytes);
+        pl.bar_off = static_cast<uint32_t>(pl.warp_off + warp_bytes);
+        pl.smem = pl.bar_off + bar_bytes + 1024;  // + alignment of the base to 1024 bytes
+        return pl;
+    }
     // shared memory: as many ring stages as fit two CTAs per SM (at most kMaxStages)
     pl.stage_bytes = static_cast<uint32_t>(4 * kTileRows * hd);  // K and V rows, packed (multiple of 128 bytes)
     const size_t q_bytes = static_cast<size_t>(kMaxHeads) * (hd + 4) * sizeof(float);
@@ -506,17 +896,38 @@ PFN_cuTensorMapEncodeTiled_v12000 attn_encode_fn() {
 
 // The cache [n_ctx][n_kv][hd] fp16 as a 3-D tensor (hd innermost); a box is
 // one KV head's hd values at kTileRows consecutive positions.
-bool encode_cache_map(CUtensorMap* map, const void* base, int n_kv, int hd, int64_t len) {
+// `box_x` head_dim values (64 with the 128-byte swizzle the MMA operand
+// layout needs, else head_dim) of `rows` positions.
+bool encode_cache_map(CUtensorMap* map, const void* base, int n_kv, int hd, int64_t len, int box_x, int rows,
+                      bool swizzle) {
     PFN_cuTensorMapEncodeTiled_v12000 encode = attn_encode_fn();
     if (encode == nullptr) return false;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(hd), static_cast<cuuint64_t>(n_kv),
                                 static_cast<cuuint64_t>(len)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(hd) * 2, static_cast<cuuint64_t>(n_kv) * hd * 2};
-    const cuuint32_t box[3] = {static_cast<cuuint32_t>(hd), 1, static_cast<cuuint32_t>(kTileRows)};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_x), 1, static_cast<cuuint32_t>(rows)};
     const cuuint32_t estr[3] = {1, 1, 1};
     return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int GP, int HD>
+cudaError_t launch_tc(const AttnPlan& pl, dim3 grid, const AttnMaps& m, const TcParams& p, cudaStream_t s) {
+    cudaError_t e = ensure_smem_attr<attn_tc_kernel<GP, HD>>();
+    if (e != cudaSuccess) return e;
+    return launch_kernel(attn_tc_kernel<GP, HD>, grid, dim3(kTcThreads), pl.smem, s, true, m.k, m.v, p);
+}
+
+template <int HD>
+cudaError_t launch_tc_hd(int gp, const AttnPlan& pl, dim3 grid, const AttnMaps& m, const TcParams& p,
+                         cudaStream_t s) {
+    switch (gp) {
+        case 1: return launch_tc<1, HD>(pl, grid, m, p, s);
+        case 2: return launch_tc<2, HD>(pl, grid, m, p, s);
+        case 4: return launch_tc<4, HD>(pl, grid, m, p, s);
+        default: return launch_tc<8, HD>(pl, grid, m, p, s);
+    }
 }
 
 }  // namespace
@@ -534,38 +945,66 @@ cudaError_t attention_run(const float* q, const void* k, const void* v, float* o
                           int64_t len, float scale, void* ws, cudaStream_t s) {
     const AttnPlan pl = plan_attn(n_q, n_kv, hd, len);
     // the ring doubles as the buffer of the warps' outputs at the end
-    if (pl.ns < 2 || static_cast<size_t>(pl.ns) * pl.stage_bytes < static_cast<size_t>(kCW) * kMaxHeads * hd * 4)
+    const int cw = pl.tc ? kTcCW : kCW;
+    if (pl.ns < 2 || pl.smem > kSmemOptin ||
+        static_cast<size_t>(pl.ns) * pl.stage_bytes < static_cast<size_t>(cw) * kMaxHeads * hd * 4)
         return cudaErrorInvalidConfiguration;
     AttnMaps maps;
-    if (!encode_cache_map(&maps.k, k, n_kv, hd, len) || !encode_cache_map(&maps.v, v, n_kv, hd, len))
+    const int box_x = pl.tc ? 64 : hd, rows = pl.tc ? kTcRows : kTileRows;
+    if (!encode_cache_map(&maps.k, k, n_kv, hd, len, box_x, rows, pl.tc) ||
+        !encode_cache_map(&maps.v, v, n_kv, hd, len, hd, rows, false))
         return cudaErrorInvalidValue;
-    AttnParams p;
-    p.q = q;
-    p.o_part = static_cast<float*>(ws);
-    p.ml_part = p.o_part + static_cast<size_t>(pl.nsplit) * n_q * hd;
-    p.len = len;
-    p.n_q = n_q;
-    p.n_kv = n_kv;
-    p.group = n_q / n_kv;
-    p.hgroups = pl.hgroups;
-    p.chunk = pl.chunk;
-    p.ns = pl.ns;
+    float* o_part = static_cast<float*>(ws);
+    float* ml_part = o_part + static_cast<size_t>(pl.nsplit) * n_q * hd;
+    const int group = n_q / n_kv;
     // scores are kept in base 2: s2 = scale * log2(e) * q.k, so exp(s - m) = 2^(s2 - m2)
-    p.scale = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-    p.stage_bytes = pl.stage_bytes;
-    p.q_off = pl.q_off;
-    p.warp_off = pl.warp_off;
-    p.bar_off = pl.bar_off;
+    const float scale2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     const dim3 grid(static_cast<unsigned>(n_kv * pl.hgroups), static_cast<unsigned>(pl.nsplit));
-    const int g = std::min(p.group, kMaxHeads);
+    const int g = std::min(group, kMaxHeads);
     const int gp = g <= 1 ? 1 : g <= 2 ? 2 : g <= 4 ? 4 : 8;
-    cudaError_t e = hd == 64    ? launch_split_e<2>(gp, pl, grid, maps, p, s)
-                    : hd == 128 ? launch_split_e<4>(gp, pl, grid, maps, p, s)
-                                : launch_split_e<8>(gp, pl, grid, maps, p, s);
+    cudaError_t e;
+    if (pl.tc) {
+        TcParams p;
+        p.q = q;
+        p.o_part = o_part;
+        p.ml_part = ml_part;
+        p.len = len;
+        p.n_q = n_q;
+        p.n_kv = n_kv;
+        p.group = group;
+        p.hgroups = pl.hgroups;
+        p.chunk = pl.chunk;
+        p.ns = pl.ns;
+        p.scale = scale2;
+        p.stage_bytes = pl.stage_bytes;
+        p.qb_off = pl.q_off;
+        p.pbuf_off = pl.pbuf_off;
+        p.warp_off = pl.warp_off;
+        p.bar_off = pl.bar_off;
+        e = hd == 64 ? launch_tc_hd<64>(gp, pl, grid, maps, p, s) : launch_tc_hd<128>(gp, pl, grid, maps, p, s);
+    } else {
+        AttnParams p;
+        p.q = q;
+        p.o_part = o_part;
+        p.ml_part = ml_part;
+        p.len = len;
+        p.n_q = n_q;
+        p.n_kv = n_kv;
+        p.group = group;
+        p.hgroups = pl.hgroups;
+        p.chunk = pl.chunk;
+        p.ns = pl.ns;
+        p.scale = scale2;
+        p.stage_bytes = pl.stage_bytes;
+        p.q_off = pl.q_off;
+        p.warp_off = pl.warp_off;
+        p.bar_off = pl.bar_off;
+        e = launch_split_e<8>(gp, pl, grid, maps, p, s);
+    }
     if (e != cudaSuccess) return e;
     const size_t msmem = (2 * static_cast<size_t>(pl.nsplit) + kMergeThreads + 8) * sizeof(float);
     return launch_kernel(attn_merge_kernel, dim3(static_cast<unsigned>(n_q)), dim3(kMergeThreads), msmem, s, true,
-                         static_cast<const float*>(p.o_part), static_cast<const float*>(p.ml_part), out, n_q, hd,
+                         static_cast<const float*>(o_part), static_cast<const float*>(ml_part), out, n_q, hd,
                          pl.nsplit);
 }
 
