@@ -718,8 +718,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (!mbar_wait_warp(&full[slot], (t / p.ns) & 1, &g_attn_err)) break;
             const uint8_t* vb = smem + static_cast<size_t>(slot) * p.stage_bytes + kVOff +
                                 static_cast<size_t>(32 * wq) * (2 * HD) + lane * (2 * E);
-            const int nrow = min(32, rows - 32 * wq);
-            for (int r = 0; r < nrow; ++r) {
+            auto value_row = [&](int r) {
                 const uint8_t* vr = vb + r * (2 * HD);
                 float2 vv[E / 2];
                 if constexpr (E == 2) {
@@ -744,6 +743,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int h = 0; h < GP; ++h)
 #pragma unroll
                     for (int e = 0; e < E / 2; ++e) acc[h][e] = __ffma2_rn(ph[h], vv[e], acc[h][e]);
+            };
+            const int nrow = min(32, rows - 32 * wq);
+            if (nrow == 32) {
+                // a full stage: unrolled, so several rows' loads are in flight at once
+#pragma unroll 8
+                for (int r = 0; r < 32; ++r) value_row(r);
+            } else {
+                for (int r = 0; r < nrow; ++r) value_row(r);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);

@@ -2,10 +2,11 @@
 
 The oracle (oracle.attention_decode) evaluates the softmax in float64 and
 returns the fp32 error bound of each output element; the kernel must land
-inside it. Cases span one position, ragged tails shorter than a 32-position
-stage, many chunks, grouped-query heads that are not a power of two, more
-than 8 query heads per KV head (two head groups), all three head sizes and
-the 32k-position workload the bench times.
+inside it. Cases span one position, ragged tails shorter than a stage (128
+positions with the tensor-core score path, 28 with the CUDA-core one), many
+chunks, grouped-query heads that are not a power of two, more than 8 query
+heads per KV head (two head groups), all three head sizes and the
+32k-position workload the bench times.
 """
 
 import numpy as np
