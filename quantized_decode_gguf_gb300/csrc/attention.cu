@@ -7,18 +7,20 @@
 //
 // with query head h reading KV head h / (n_q / n_kv). Split-KV ("flash
 // decode") in two kernels:
-//  1. attn_split_kernel, grid (KV head x group of at most 8 query heads,
-//     position chunk). A producer thread streams the chunk's K and V rows
-//     through a ring of 28-position stages, one 3-D tensor copy (TMA) per
-//     stage for K and one for V (the rows of one KV head are strided in the
-//     cache; small per-row copies measured far below HBM speed);
-//     each of 7 consumer warps owns 4 positions of every stage and keeps its
-//     own online-softmax state (running maximum m, exp-sum l and
-//     o = sum_j e^(s_j - m) v_j per query head). At the end the warps' states
-//     are combined in warp order into the chunk's (m, l, o). Scores take 8
-//     lanes per position, each lane a fixed set of 16-byte chunks of the key
-//     for every query head of the CTA (the CTA's head count is a template
-//     argument, so these loops unroll).
+//  1. Split pass, grid (KV head x group of at most 8 query heads, position
+//     chunk). A producer thread streams the chunk's K and V rows through a
+//     shared-memory ring with 3-D tensor copies (TMA) of one KV head's rows
+//     (they are strided in the cache; small per-row copies measured far
+//     below HBM speed). Consumer warps keep per-warp online-softmax states
+//     (running maximum m, exp-sum l and o = sum_j e^(s_j - m) v_j per query
+//     head), combined in warp order into the chunk's (m, l, o). Two score
+//     paths:
+//     - attn_tc_kernel (head_dim 64, 128): the scores of a 128-position
+//       stage are a tcgen05 MMA (see the section below);
+//     - attn_split_kernel (head_dim 256): 28-position stages, 8 lanes per
+//       position, each lane a fixed set of 16-byte chunks of the key for
+//       every query head of the CTA, on the CUDA cores.
+//     The CTA's head count is a template argument, so the head loops unroll.
 //  2. attn_merge_kernel, one CTA per query head: out = sum_c e^(m_c - M) o_c /
 //     sum_c e^(m_c - M) l_c over the chunks c in order (M their maximum).
 // Scores and maxima are held in base 2 (scale folded with log2 e), so every

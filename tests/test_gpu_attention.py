@@ -53,6 +53,9 @@ CASES = [
     (300, 8, 8, 256),       # one query head per KV head
     (5000, 4, 2, 256),
     (32768, 16, 4, 128),    # the depth-32k workload
+    (1500, 8, 8, 128),      # one query head per KV head on the tensor-core path
+    (700, 4, 2, 64),        # two query heads per KV head, head_dim 64
+    (1200, 16, 2, 256),     # eight query heads per KV head, head_dim 256
 ]
 
 
