@@ -219,9 +219,14 @@ def prefill_gemm(w: np.ndarray, x: np.ndarray):
 # ----------------------------------------------------------------------------
 
 def silu(g: np.ndarray) -> np.ndarray:
-    """g / (1 + exp(-g)) in float64."""
+    """g / (1 + exp(-g)) in float64.
+
+    For g below about -709, exp(-g) overflows to inf and the quotient is the
+    correct limit -0.0; numpy's overflow warning for that case is silenced.
+    """
     g = np.asarray(g, dtype=np.float64)
-    return g / (1.0 + np.exp(-g))
+    with np.errstate(over="ignore"):
+        return g / (1.0 + np.exp(-g))
 
 
 SILU_SLOPE_MAX = 1.1  # max |d silu / dg| = 1.0998..., rounded up
