@@ -146,6 +146,11 @@ phb_status phb_ffn_swiglu(int qtype, const void* Wgate, const void* Wup, const v
  * Y: [n_tokens][d_model]. out_idx ([n_tokens][top_k] int32) and out_p
  * ([n_tokens][top_k] fp32) receive the routing in descending logit order
  * when not NULL. n_tokens 1..64, n_experts 1..256, top_k 1..min(8, n_experts).
+ * The workspace carries per-row-tile counters (one or two tokens: the last
+ * CTA of a tile combines the slots): zero it before the first call and pass
+ * the same, otherwise untouched, workspace to later calls (each call returns
+ * the counters to zero); calls sharing a workspace must not overlap on the
+ * GPU. After a device error (phb_device_error) zero it again.
  * ------------------------------------------------------------------------- */
 size_t phb_moe_ffn_workspace_size(int qtype, int64_t n_tokens, int64_t d_model, int64_t d_ff,
                                   int n_experts, int top_k);

@@ -13,8 +13,10 @@
 //    and writes h[pair] = silu(gate.x) * (up.x).
 // 3. moe_rows_kernel<NMAT=1>: the same over 128 rows of the down matrices,
 //    x = h[pair], writing y_pair[pair].
-// 4. moe_combine_kernel: y[t] = sum over slots (ascending) of p[t][slot] *
-//    y_pair[t*top_k + slot].
+// 4. The ordered combine y[t] = sum over slots (ascending) of p[t][slot] *
+//    y_pair[t*top_k + slot]: for one or two tokens the last down-pass CTA of
+//    each 128-row tile does it (a per-tile counter in the workspace, back to
+//    zero after each call); for more tokens moe_combine_kernel.
 // All orders are fixed, so repeated calls give identical bits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -297,6 +299,10 @@ struct MoeRowsParams {
     int32_t* out_idx;
     float* out_p;
     int route_inline;  // gate/up pass: 1 = route in the kernel, 0 = read the routing kernel's lists
+    // down pass: 1 = the last CTA of a row tile combines the slots into y_out
+    int combine;
+    int* tile_ctr;     // [row tiles], zero between calls
+    float* y_out;      // Y [n_tokens][n]
 };
 
 __device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* map, int x, int y, int z,
@@ -464,6 +470,30 @@ __global__ void __launch_bounds__(kMrThreads, 1)
             ok = moe_rows_group<QT, NMAT, 4>(p, plist, row0, fp, nb, smem, full, empty, s);
         if (!ok) return;
     }
+    if constexpr (NMAT == 1) {
+        if (p.combine) {
+            // the last CTA of this row tile to publish its pairs sums the slots in ascending order
+            int* flag = reinterpret_cast<int*>(smem + p.route_off);  // the routing area is unused here
+            __threadfence();
+            consumer_sync<kMrNC>();
+            if (tid == 0) *flag = atomicAdd(p.tile_ctr + blockIdx.x, 1) == n_active - 1 ? 1 : 0;
+            consumer_sync<kMrNC>();
+            if (*flag) {
+                __threadfence();
+                for (int i = tid; i < p.n_tokens * kMrRows; i += kMrNC) {
+                    const int t = i / kMrRows, r = i - t * kMrRows;
+                    const int64_t n = row0 + r;
+                    if (n >= p.n) continue;
+                    float acc = 0.f;
+                    for (int k = 0; k < p.top_k; ++k)
+                        acc = fmaf(__ldcg(p.r.p + t * p.top_k + k),
+                                   __ldcg(p.y + static_cast<int64_t>(t * p.top_k + k) * p.ldy + n), acc);
+                    p.y_out[static_cast<int64_t>(t) * p.n + n] = acc;
+                }
+                if (tid == 0) p.tile_ctr[blockIdx.x] = 0;
+            }
+        }
+    }
     if (tid == 0) PHB_TRACE_EV(p.trace_id, 3);
 }
 
@@ -532,6 +562,7 @@ struct MoeWs {
     RouteOut r;
     float* h;
     float* yp;
+    int* tile_ctr;  // down-pass row tiles: combine counters
     size_t bytes;
 };
 
@@ -557,6 +588,7 @@ MoeWs moe_ws_layout(const MoeReq& q, void* base) {
     w.r.pair_list = reinterpret_cast<int32_t*>(take(pairs * 4));
     w.h = reinterpret_cast<float*>(take(pairs * q.d_ff * 4));
     w.yp = reinterpret_cast<float*>(take(pairs * q.d_model * 4));
+    w.tile_ctr = reinterpret_cast<int*>(take(static_cast<size_t>((q.d_model + kMrRows - 1) / kMrRows) * 4));
     w.bytes = off;
     return w;
 }
@@ -625,10 +657,14 @@ cudaError_t moe_run(const MoeReq& q, cudaStream_t s) {
         pd.units_row = static_cast<int>(q.d_ff / kUnitWeights);
         pd.row_tile = kMrRows;
         pd.trace_id = tb + 2;
+        pd.combine = inline_route ? 1 : 0;  // one or two tokens: the combine is a few loads per output
+        pd.tile_ctr = w.tile_ctr;
+        pd.y_out = q.y;
+        pd.n_tokens = static_cast<int>(q.t);
         if (smem_d > kSmemOptin) return cudaErrorInvalidConfiguration;
         const dim3 gd(static_cast<unsigned>(cdiv(q.d_model, kMrRows)), static_cast<unsigned>(slots));
         e = q.qt == 0 ? launch_moe_rows<0, 1>(td, td, pd, gd, smem_d, s) : launch_moe_rows<1, 1>(td, td, pd, gd, smem_d, s);
-        if (e != cudaSuccess) return e;
+        if (e != cudaSuccess || pd.combine) return e;
         const int64_t total = q.t * q.d_model;
         return launch_kernel(moe_combine_kernel, dim3(static_cast<unsigned>(cdiv(total, 256))), dim3(256), 0, s, true,
                              static_cast<const float*>(w.yp), static_cast<const float*>(w.r.p), q.y,
