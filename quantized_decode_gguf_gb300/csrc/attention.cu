@@ -54,9 +54,10 @@ cudaError_t read_dev_err_attention(int* code) {
 
 namespace {
 
-// 7 consumer warps + 1 producer warp: two CTAs (16 warps) per SM leave 128
-// registers a thread (register files are split between an SM's 4
-// schedulers), enough to keep the query values in registers.
+// CUDA-core score path (head_dim 256). 7 consumer warps + 1 producer warp:
+// two CTAs (16 warps) per SM leave 128 registers a thread (register files
+// are split between an SM's 4 schedulers), enough to keep the query values
+// in registers.
 constexpr int kCW = 7;                // consumer warps, 4 positions of each stage apiece
 constexpr int kTileRows = 4 * kCW;    // positions per ring stage
 constexpr int kNC = 32 * kCW;
@@ -75,8 +76,9 @@ struct AttnParams {
     uint32_t stage_bytes, q_off, warp_off, bar_off;
 };
 
-// One box of the [n_ctx][n_kv][head_dim] cache: head_dim x 1 KV head x
-// kTileRows positions, landing as kTileRows packed rows.
+// One box of the [n_ctx][n_kv][head_dim] cache at (element x, KV head y,
+// position z): the map's box width x 1 KV head x its positions, landing as
+// packed rows (swizzled when the map says so).
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar,
                                             uint64_t policy) {
     asm volatile(
