@@ -239,8 +239,11 @@ phb_status phb_decode_step_unfused(int qtype, const phb_dense_layer* layers, int
  * within the fp32 error bound of the exact softmax and bitwise identical
  * across calls. K and V are read once (query heads past 8 per KV head
  * re-read them from L2).
- * Needs n_q_heads % n_kv_heads == 0, head_dim 64, 128 or 256 and
- * 1 <= n_ctx <= 2^26; every pointer 16-byte aligned. The workspace holds
+ * Needs n_q_heads % n_kv_heads == 0 and head_dim 64, 128 or 256
+ * (PHB_ERR_SHAPE), 1 <= n_ctx <= 2^26, positive head counts and a finite
+ * scale (PHB_ERR_INVALID_ARG), every pointer 16-byte aligned
+ * (PHB_ERR_ALIGN) and ws_bytes >= the workspace size (PHB_ERR_WORKSPACE);
+ * a call that fails these launches nothing. The workspace holds
  * one partial result per position chunk; its size depends on the current
  * device's SM count. Nothing in it needs to start at zero.
  * ------------------------------------------------------------------------- */
