@@ -235,9 +235,11 @@ phb_status phb_decode_step_unfused(int qtype, const phb_dense_layer* layers, int
  * q: [n_q_heads][head_dim] fp32; k_cache, v_cache: [n_ctx][n_kv_heads]
  * [head_dim] IEEE fp16 (the first n_ctx positions of a cache in that
  * layout); out: [n_q_heads][head_dim] fp32. scale is usually
- * 1/sqrt(head_dim). Scores, exponentials and sums are fp32; the result is
- * within the fp32 error bound of the exact softmax and bitwise identical
- * across calls. K and V are read once (query heads past 8 per KV head
+ * 1/sqrt(head_dim). Scores are accumulated in fp32 (for head_dim 64 and
+ * 128 on the tensor cores, from the fp16 keys and the query split into two
+ * fp16 parts after a per-head power-of-two scaling, about 2^-22 relative);
+ * exponentials and sums are fp32. The result is within the fp32 error bound
+ * of the exact softmax and bitwise identical across calls. K and V are read once (query heads past 8 per KV head
  * re-read them from L2).
  * Needs n_q_heads % n_kv_heads == 0 and head_dim 64, 128 or 256
  * (PHB_ERR_SHAPE), 1 <= n_ctx <= 2^26, positive head counts and a finite
