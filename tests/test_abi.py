@@ -127,3 +127,16 @@ def test_attention_rejects_bad_arguments(lib):
     assert lib.phb_attention_decode_workspace_size(4096, 16, 4, 80) == 0
     assert lib.phb_attention_decode_workspace_size(0, 16, 4, 128) == 0
     assert lib.phb_attention_decode_workspace_size(4096, 16, 5, 128) == 0
+
+
+def test_attention_binding_rejects_a_non_fp16_cache():
+    # the binding checks the cache dtype before it touches the library or a device
+    import torch
+
+    import quantized_decode_gguf_gb300 as phb
+    q = torch.zeros(8, 64)
+    k32 = torch.zeros(16, 2, 64)
+    with pytest.raises(TypeError):
+        phb.attention_decode(q, k32, k32.half(), 16, 8, 2, 64)
+    with pytest.raises(TypeError):
+        phb.attention_decode(q, k32.half(), k32, 16, 8, 2, 64)
