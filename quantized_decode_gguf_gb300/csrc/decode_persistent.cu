@@ -11,7 +11,7 @@
 //
 // Activations stay in registers. A consumer thread owns one fixed half-unit
 // position (128 consecutive k) of the GEMV's rows and keeps those 128 scaled
-// activations (and their four 32-sums) in registers for the whole GEMV, so
+// activations in registers for the whole GEMV, so
 // per weight only the quantized bytes come from shared memory. A stage holds
 // whole row segments: with useg units per row segment, a stage carries
 // floor(128 / (nmat * useg)) * nmat segments and thread t works on segment
@@ -101,7 +101,7 @@ struct PersistParams {
     uint2* xl[2];
     int64_t rs_qkv, rs_dm, rs_ff;  // replica strides (pairs) of qkv, the d_model vectors, act
     unsigned* state;
-    uint32_t xs_off, xsum_off, part_off, res_off, bar_off;
+    uint32_t xs_off, part_off, res_off, bar_off;
 };
 
 template <int QT, int NS>
@@ -109,7 +109,6 @@ __global__ void __launch_bounds__(KCfg<QT, kCW>::threads, 1) decode_persistent_k
     using C = KCfg<QT, kCW, NS>;
     extern __shared__ __align__(1024) uint8_t smem[];
     float* xs = reinterpret_cast<float*>(smem + p.xs_off);
-    float* xsum = reinterpret_cast<float*>(smem + p.xsum_off);
     float* part = reinterpret_cast<float*>(smem + p.part_off);
     float* res = reinterpret_cast<float*>(smem + p.res_off);
     float* rsum = res + kNC;  // NMAT * rows_here row sums
@@ -127,7 +126,7 @@ __global__ void __launch_bounds__(KCfg<QT, kCW>::threads, 1) decode_persistent_k
     const int tid = threadIdx.x;
     const int nctas = gridDim.x;
     const int n_ops = 4 * p.n_layers;
-    const StageCtx sctx{p.state, p.n_q, p.n_kv, p.head_dim, nullptr, 1};
+    const StageCtx sctx{p.state, p.n_q, p.n_kv, p.head_dim};
     if (tid == 0) {
         for (int s = 0; s < C::ns; ++s) {
             mbar_init(&full[s], 1);
@@ -213,20 +212,20 @@ __global__ void __launch_bounds__(KCfg<QT, kCW>::threads, 1) decode_persistent_k
             bool ok;
             switch (j) {
                 case 0:
-                    ok = stage_vec<1>(sctx, lin_t, lin_p, tag_lin, kseg, xs, xsum, xfac, red, flag, nullptr, nullptr, 0,
+                    ok = stage_vec<1>(sctx, lin_t, lin_p, tag_lin, kseg, xs, xfac, red, flag, nullptr, nullptr, 0,
                                       res, 0, retries, op);
                     break;
                 case 1:
-                    ok = stage_vec<2>(sctx, p.qkv + rep * p.rs_qkv, nullptr, tag_prev, kseg, xs, xsum, xfac, red, flag,
+                    ok = stage_vec<2>(sctx, p.qkv + rep * p.rs_qkv, nullptr, tag_prev, kseg, xs, xfac, red, flag,
                                       lin_t ? lin_t + row0 : nullptr, lin_p ? lin_p + row0 : nullptr, tag_lin, res,
                                       t.rows_here, retries, op);
                     break;
                 case 2:
-                    ok = stage_vec<1>(sctx, p.x1 + rep * p.rs_dm, nullptr, tag_prev, kseg, xs, xsum, xfac, red, flag, nullptr, nullptr, 0,
+                    ok = stage_vec<1>(sctx, p.x1 + rep * p.rs_dm, nullptr, tag_prev, kseg, xs, xfac, red, flag, nullptr, nullptr, 0,
                                       res, 0, retries, op);
                     break;
                 default:
-                    ok = stage_vec<0>(sctx, p.act + rep * p.rs_ff, nullptr, tag_prev, kseg, xs, xsum, xfac, red, flag,
+                    ok = stage_vec<0>(sctx, p.act + rep * p.rs_ff, nullptr, tag_prev, kseg, xs, xfac, red, flag,
                                       p.x1 + rep * p.rs_dm + row0,
                                       nullptr, tag_me - 2, res, t.rows_here, retries, op);
                     break;
@@ -234,8 +233,8 @@ __global__ void __launch_bounds__(KCfg<QT, kCW>::threads, 1) decode_persistent_k
             alive = ok;
         }
         if (tid == 0) PHB_TRACE_EV(op, 2);
-        // this thread's half-unit position: activations and 32-sums into registers
-        float xr[kHalfK], xsr[4];
+        // this thread's half-unit position: activations into registers
+        float xr[kHalfK];
         {
             const int pos = tid % (2 * t.useg);
             const float* xp = xs + pos * (kXPadEvery + kXPad);
@@ -247,8 +246,6 @@ __global__ void __launch_bounds__(KCfg<QT, kCW>::threads, 1) decode_persistent_k
                 xr[i + 2] = v.z;
                 xr[i + 3] = v.w;
             }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) xsr[i] = xsum[4 * pos + i];
         }
         const float xf = xfac[0];
         const bool last = (l == p.n_layers - 1);
@@ -273,9 +270,9 @@ __global__ void __launch_bounds__(KCfg<QT, kCW>::threads, 1) decode_persistent_k
         // on abort the stages are still drained (no copy may be left in flight)
         bool ok;
         if (nmat == 2)
-            ok = consume_xr<QT, 2, NS>(t, segs, smem, full, empty, s, xr, xsr, xf, part, rsum, alive, op, epi);
+            ok = consume_xr<QT, 2, NS>(t, segs, smem, full, empty, s, xr, xf, part, rsum, alive, op, epi);
         else
-            ok = consume_xr<QT, 1, NS>(t, segs, smem, full, empty, s, xr, xsr, xf, part, rsum, alive, op, epi);
+            ok = consume_xr<QT, 1, NS>(t, segs, smem, full, empty, s, xr, xf, part, rsum, alive, op, epi);
         alive = alive && ok;
         consumer_sync<kNC>();
         if (tid == 0) {
@@ -396,7 +393,6 @@ cudaError_t decode_persistent_run(int qt, const void* const* wl, int n_layers, i
         ns = cand;
         smem = total;
         p.xs_off = lay.xs;
-        p.xsum_off = lay.xsum;
         p.part_off = lay.part;
         p.res_off = static_cast<uint32_t>(res_off);
         p.bar_off = static_cast<uint32_t>(bar_off);

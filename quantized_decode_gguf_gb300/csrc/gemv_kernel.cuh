@@ -162,8 +162,7 @@ __device__ __forceinline__ bool produce_tile(const Tile& t, int nmat, uint8_t* s
 template <int QT, int CW, int MAXB, int NMAT, int NS = KCfg<QT, CW>::ns, class EpiF>
 __device__ __forceinline__ bool consume_tile(const Tile& t, int mode, const uint8_t* stages, uint64_t* full,
                                              uint64_t* empty, int& s, const float* xs, int xstride,
-                                             const float* xsum, int sstride, const float* xfac, int batch,
-                                             float* part, float* row_acc, EpiF epi) {
+                                             const float* xfac, int batch, float* part, float* row_acc, EpiF epi) {
     using C = KCfg<QT, CW, NS>;
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -189,11 +188,10 @@ __device__ __forceinline__ bool consume_tile(const Tile& t, int mode, const uint
             const int hu = 2 * u + hsel;  // half unit within the row segment
             const uint8_t* ub = stages + slot * C::stage_bytes + ulocal * C::ub;
             const float* xsp = xs + hu * (kXPadEvery + kXPad);
-            const float* xsm = xsum + hu * 4;
             if constexpr (QT == 0)
-                dot_q8_0_half<MAXB>(ub + 136 * hsel, xsp, xstride, xsm, sstride, xfac, acc);
+                dot_q8_0_half<MAXB>(ub + 136 * hsel, xsp, xstride, xfac, acc);
             else
-                dot_q4_k_half<MAXB>(ub, hsel, xsp, xstride, xsm, sstride, xfac, acc);
+                dot_q4_k_half<MAXB>(ub, hsel, xsp, xstride, xfac, acc);
         }
         if (mode == kSumWarp) {
             float other[MAXB];
@@ -280,33 +278,34 @@ __device__ __forceinline__ bool consume_tile(const Tile& t, int mode, const uint
 
 // Stage activations a[b][0 .. kseg) for b < batch into shared memory:
 //   xs   [MAXB][xpad_len(kseg)]: a * 2^s_b in the padded layout (xpad_idx)
-//   xsum [MAXB][kseg/32]:        sums of every 32 consecutive a
-//   xfac [MAXB]:                 2^(149 - s_b)
+//   xfac [MAXB]:                 2^(kWShift - s_b)
 // Rows batch..MAXB-1 are zero (xfac 1). a is x[b][kbase + k] (kXPlain),
 // x[rowidx[b]][k] (kXRowList), the V head of the query head that owns k
 // (kXGatherV), or x[b][k] * r_b with r_b = (mean_k x^2 + eps)^-1/2
 // (kXRmsNorm; rows are whole). s_b is chosen from max|a| so that
-// |a| * 2^s_b < 2^125. One global read pass, three consumer barriers.
+// |a| * 2^s_b < 2^125: the scaled weights are below 2^-58, so no product
+// or sum of up to 2^20 products can overflow, and no product of a weight
+// with an activation of more than 2^-140 times the row's largest magnitude
+// can underflow. One global read pass, three consumer barriers.
 // `red` needs (2 * CW + 3) * kAccStride floats.
-// Capped at 254 so that 2^s splits into two finite factors 2^min(s,127) and
-// 2^(s-127) and 2^(149-s) stays a normal number (vectors whose largest
-// magnitude is below 2^-129 are scaled by 2^254, still below 2^125).
+// Capped at kWShift + 126 so that 2^(kWShift - s) stays a normal number
+// (vectors whose largest magnitude is below 2^-86 are scaled by 2^211,
+// still below 2^125); s >= -3 for every finite vector.
 __device__ __forceinline__ int pick_scale_exp(float amax) {
     if (!(amax > 0.f) || !isfinite(amax)) return 125;
     const int e = ilogbf(amax) + 1;  // amax < 2^e
-    return min(254, max(22, 125 - e));
+    return min(kWShift + 126, 125 - e);
 }
 
 template <int CW, int MAXB, int XMODE>
 __device__ __forceinline__ void stage_x(const float* x, int64_t ldx, int64_t kbase, int kseg, int batch, float* xs,
-                                       float* xsum, float* xfac, float* red, int gather_group, int gather_hd,
+                                       float* xfac, float* red, int gather_group, int gather_hd,
                                        int64_t gather_v_off, const int* rowidx = nullptr) {
     constexpr int NC = 32 * CW;
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int xstride = xpad_len(kseg);
-    const int nch = kseg / 8;  // 8-float chunks per row; kseg % 32 == 0, so groups of 4 chunks make a 32-sum
-    const int nsub = kseg / 32;
+    const int nch = kseg / 8;  // 8-float chunks per row
     float ssq[MAXB], mx[MAXB];
 #pragma unroll
     for (int b = 0; b < MAXB; ++b) ssq[b] = mx[b] = 0.f;
@@ -344,7 +343,6 @@ __device__ __forceinline__ void stage_x(const float* x, int64_t ldx, int64_t kba
         float* dst = xs + b * xstride + xpad_idx(8 * c);
         *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
         *reinterpret_cast<float4*>(dst + 4) = make_float4(v[4], v[5], v[6], v[7]);
-        float cs = ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
         const float cm = fmaxf(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))),
                                fmaxf(fmaxf(fabsf(v[4]), fabsf(v[5])), fmaxf(fabsf(v[6]), fabsf(v[7]))));
         float cq = 0.f;
@@ -352,11 +350,6 @@ __device__ __forceinline__ void stage_x(const float* x, int64_t ldx, int64_t kba
 #pragma unroll
             for (int e = 0; e < 8; ++e) cq = fmaf(v[e], v[e], cq);
         }
-        // 32-sum over the 4 consecutive lanes holding one 32-weight block
-        const unsigned gmask = 0xFu << (lane & 28);
-        cs += __shfl_xor_sync(gmask, cs, 1);
-        cs += __shfl_xor_sync(gmask, cs, 2);
-        if ((lane & 3) == 0) xsum[b * nsub + (c >> 2)] = cs;
 #pragma unroll
         for (int bb = 0; bb < MAXB; ++bb) {
             if (bb == b) {
@@ -396,7 +389,7 @@ __device__ __forceinline__ void stage_x(const float* x, int64_t ldx, int64_t kba
         rfac[tid] = r;
         f1[tid] = ldexpf(1.0f, e1);
         f2[tid] = ldexpf(1.0f, se - e1);
-        xfac[tid] = tid < batch ? ldexpf(1.0f, 149 - se) : 1.0f;
+        xfac[tid] = tid < batch ? ldexpf(1.0f, kWShift - se) : 1.0f;
     }
     consumer_sync<NC>();
     const int per_row4 = kseg / 4;
@@ -417,9 +410,6 @@ __device__ __forceinline__ void stage_x(const float* x, int64_t ldx, int64_t kba
         v.z = v.z * a * c;
         v.w = v.w * a * c;
         *p = v;
-    }
-    if constexpr (XMODE == kXRmsNorm) {
-        for (int i = tid; i < batch * nsub; i += NC) xsum[i] *= rfac[i / nsub];
     }
     consumer_sync<NC>();
 }
@@ -450,7 +440,7 @@ struct GemvParams {
     int64_t gather_v_off;  // kXGatherV: offset of V in the qkv vector
     const uint8_t* pf[2];  // weights of later kernels to prefetch into L2 (optional)
     int64_t pf_bytes[2];
-    uint32_t xs_off, xsum_off, part_off, acc_off, bar_off;  // dynamic shared memory layout
+    uint32_t xs_off, part_off, acc_off, bar_off;  // dynamic shared memory layout
     int trace_id;          // launch id for debug tracing builds (-1: none)
 };
 
@@ -462,7 +452,6 @@ __global__ void __launch_bounds__(KCfg<QT, CW>::threads, MAXB <= 2 ? 2 : 1)
     using C = KCfg<QT, CW>;
     extern __shared__ __align__(1024) uint8_t smem[];
     float* xs = reinterpret_cast<float*>(smem + p.xs_off);
-    float* xsum = reinterpret_cast<float*>(smem + p.xsum_off);
     float* part = reinterpret_cast<float*>(smem + p.part_off);
     float* row_acc = reinterpret_cast<float*>(smem + p.acc_off);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
@@ -515,7 +504,7 @@ __global__ void __launch_bounds__(KCfg<QT, CW>::threads, MAXB <= 2 ? 2 : 1)
 
     pdl_wait();
     if (tid == 0) PHB_TRACE_EV(p.trace_id, 1);
-    stage_x<CW, MAXB, XMODE>(p.x, p.ldx, static_cast<int64_t>(u0) * kUnitWeights, kseg, batch, xs, xsum, xfac, red,
+    stage_x<CW, MAXB, XMODE>(p.x, p.ldx, static_cast<int64_t>(u0) * kUnitWeights, kseg, batch, xs, xfac, red,
                              p.gather_group, p.gather_hd, p.gather_v_off);
     if (tid == 0) PHB_TRACE_EV(p.trace_id, 2);
     const bool split_out = gridDim.y > 1;
@@ -538,8 +527,8 @@ __global__ void __launch_bounds__(KCfg<QT, CW>::threads, MAXB <= 2 ? 2 : 1)
         PHB_TRACE_EV(p.trace_id, 3);
     }
 #endif
-    consume_tile<QT, CW, MAXB, NMAT>(t, p.sum_mode, smem, full, empty, s, xs, xpad_len(kseg), xsum, kseg / 32, xfac,
-                                     batch, part, row_acc, epi);
+    consume_tile<QT, CW, MAXB, NMAT>(t, p.sum_mode, smem, full, empty, s, xs, xpad_len(kseg), xfac, batch, part,
+                                     row_acc, epi);
     if (tid == 0) PHB_TRACE_EV(p.trace_id, 4);
 }
 

@@ -35,11 +35,11 @@ inline int plan_ksplit(const GemvReq& q) {
 constexpr int cw_for(int maxb) { return maxb <= 2 ? 8 : maxb <= 4 ? 12 : 11; }
 
 // Dynamic shared memory of a streaming-GEMV CTA:
-//   stages | xs [maxb][xpad_len(kseg)] | xsum [maxb][kseg/32] |
+//   stages | xs [maxb][xpad_len(kseg)] |
 //   part (row-sum mode dependent) | row_acc [nmat*rows][kAccStride] (fold) |
 //   mbarriers | xfac, reduction scratch, row list
 struct SmemLayout {
-    uint32_t xs, xsum, part, acc, bar;
+    uint32_t xs, part, acc, bar;
     size_t total;
     int sum_mode;
 };
@@ -61,8 +61,6 @@ inline SmemLayout stream_smem_layout(int qt, int cw, int nmat, int maxb, int row
     const size_t kseg = static_cast<size_t>(units_seg) * kUnitWeights;
     l.xs = static_cast<uint32_t>(off);
     off += static_cast<size_t>(maxb) * xpad_len(static_cast<int>(kseg)) * sizeof(float);
-    l.xsum = static_cast<uint32_t>(off);
-    off += static_cast<size_t>(maxb) * (kseg / 32) * sizeof(float);
     l.part = static_cast<uint32_t>(off);
     const size_t tile_part = 2 * static_cast<size_t>(nmat) * rows_per_cta * units_seg * maxb * sizeof(float);
     if (warp_rows(units_seg, nmat)) {
@@ -131,7 +129,6 @@ inline bool plan_stream(const GemvReq& q, GemvPlan* pl, int ctas_per_sm = kCtasP
         p.pf_bytes[i] = q.pf_bytes[i];
     }
     p.xs_off = lay.xs;
-    p.xsum_off = lay.xsum;
     p.part_off = lay.part;
     p.acc_off = lay.acc;
     p.bar_off = lay.bar;

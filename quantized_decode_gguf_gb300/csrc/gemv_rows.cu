@@ -14,8 +14,8 @@
 // traffic no longer scales with the rows, and no cross-thread row reduction
 // is needed; the two halves of a row meet once at the end.
 //
-// The dequantize-and-dot arithmetic (exact byte-to-float conversion,
-// power-of-two activation scaling, packed FMAs) is gemv_core.cuh's.
+// The dequantize-and-dot arithmetic (exact scaled weights, power-of-two
+// activation scaling, packed FMAs) is gemv_core.cuh's.
 // K splits write partials reduced in split order by splitk_reduce_kernel,
 // so results are deterministic.
 #include <cuda.h>
@@ -63,7 +63,7 @@ struct RowsParams {
     int64_t n;
     int units_row, units_per_split;
     int batch;
-    uint32_t xs_off, xsum_off, comb_off, bar_off;
+    uint32_t xs_off, comb_off, bar_off;
 };
 
 __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
@@ -81,7 +81,6 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
     using R = RowsCfg<QT>;
     extern __shared__ __align__(1024) uint8_t smem[];
     float* xs = reinterpret_cast<float*>(smem + p.xs_off);
-    float* xsum = reinterpret_cast<float*>(smem + p.xsum_off);
     float* comb = reinterpret_cast<float*>(smem + p.comb_off);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
     uint64_t* empty = full + R::ns;
@@ -126,11 +125,11 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
     // ---------------- consumers
     pdl_wait();  // x may come from the previous kernel
     const int kseg = nst * kUnitWeights;
-    stage_x<kRowsCW, MAXB, kXPlain>(p.x, p.ldx, static_cast<int64_t>(u0) * kUnitWeights, kseg, p.batch, xs, xsum,
-                                    xfac, red, 1, 1, 0);
+    stage_x<kRowsCW, MAXB, kXPlain>(p.x, p.ldx, static_cast<int64_t>(u0) * kUnitWeights, kseg, p.batch, xs, xfac,
+                                    red, 1, 1, 0);
     const int row = tid & (kRows - 1);
     const int h = tid >> 7;  // half unit; uniform per warp, so activation loads are broadcasts
-    const int xstride = xpad_len(kseg), sstride = kseg / 32;
+    const int xstride = xpad_len(kseg);
     float acc[MAXB];
 #pragma unroll
     for (int b = 0; b < MAXB; ++b) acc[b] = 0.f;
@@ -148,11 +147,10 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
         const uint8_t* ub = smem + slot * R::stage_bytes + row * R::ub;
         const int hu = 2 * st + h;
         const float* xsp = xs + hu * (kXPadEvery + kXPad);
-        const float* xsm = xsum + hu * 4;
         if constexpr (QT == 0)
-            dot_q8_0_half<MAXB>(ub + 136 * h, xsp, xstride, xsm, sstride, xfac, acc);
+            dot_q8_0_half<MAXB>(ub + 136 * h, xsp, xstride, xfac, acc);
         else
-            dot_q4_k_half<MAXB>(ub, h, xsp, xstride, xsm, sstride, xfac, acc);
+            dot_q4_k_half<MAXB>(ub, h, xsp, xstride, xfac, acc);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
     }
@@ -197,7 +195,7 @@ PFN_cuTensorMapEncodeTiled_v12000 rows_encode_fn() {
 struct RowsPlan {
     int ksplit = 1, units_per_split = 0;
     size_t smem = 0;
-    uint32_t xs_off = 0, xsum_off = 0, comb_off = 0, bar_off = 0;
+    uint32_t xs_off = 0, comb_off = 0, bar_off = 0;
 };
 
 // Splits of K: enough CTAs to cover the SMs once (the kernel fills an SM),
@@ -208,7 +206,7 @@ RowsPlan plan_rows(int qt, int64_t n, int64_t k, int batch) {
     const int64_t tiles = cdiv(n, kRows);
     const int sms = device_sm_count();
     int ksplit = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(units_row, sms / std::max<int64_t>(1, tiles))));
-    const size_t x_per_unit = static_cast<size_t>(maxb) * (xpad_len(kUnitWeights) + kUnitWeights / 32) * 4;
+    const size_t x_per_unit = static_cast<size_t>(maxb) * xpad_len(kUnitWeights) * 4;
     const int max_units = std::max(1, static_cast<int>(kRowsXBudget / x_per_unit));
     ksplit = std::max(ksplit, static_cast<int>(cdiv(units_row, max_units)));
     RowsPlan pl;
@@ -220,8 +218,6 @@ RowsPlan plan_rows(int qt, int64_t n, int64_t k, int batch) {
     size_t off = ns * stage;
     pl.xs_off = static_cast<uint32_t>(off);
     off += static_cast<size_t>(maxb) * xpad_len(kseg) * 4;
-    pl.xsum_off = static_cast<uint32_t>(off);
-    off += static_cast<size_t>(maxb) * (kseg / 32) * 4;
     pl.comb_off = static_cast<uint32_t>(off);
     off += static_cast<size_t>(maxb) * kRows * 4;
     off = (off + 15) & ~size_t{15};
@@ -279,7 +275,6 @@ cudaError_t gemv_rows_run(const GemvReq& q, cudaStream_t s, int* ksplit_out) {
     p.units_per_split = pl.units_per_split;
     p.batch = q.batch;
     p.xs_off = pl.xs_off;
-    p.xsum_off = pl.xsum_off;
     p.comb_off = pl.comb_off;
     p.bar_off = pl.bar_off;
     const dim3 grid(static_cast<unsigned>(cdiv(q.n, kRows)), static_cast<unsigned>(pl.ksplit));

@@ -291,7 +291,7 @@ struct MoeRowsParams {
     int64_t n;             // rows per expert matrix
     int units_row;
     int row_tile;          // rows of each matrix per CTA: 64 (gate/up) or 128 (down)
-    uint32_t xs_off, xsum_off, comb_off, bar_off, route_off;
+    uint32_t xs_off, comb_off, bar_off, route_off;
     int trace_id;
     // gate/up pass: the routing is computed in the kernel from the logits
     const float* logits;
@@ -322,7 +322,6 @@ __device__ __forceinline__ bool moe_rows_group(const MoeRowsParams& p, const int
                                                int nb, uint8_t* smem, uint64_t* full, uint64_t* empty, int& s) {
     using R = MrCfg<QT>;
     float* xs = reinterpret_cast<float*>(smem + p.xs_off);
-    float* xsum = reinterpret_cast<float*>(smem + p.xsum_off);
     float* comb = reinterpret_cast<float*>(smem + p.comb_off);  // [2][MAXB][128]
     float* xfac = reinterpret_cast<float*>(full + 2 * R::ns);
     float* red = xfac + kAccStride;
@@ -334,10 +333,10 @@ __device__ __forceinline__ bool moe_rows_group(const MoeRowsParams& p, const int
         rowidx[tid] = p.x_by_pair ? pair : pair / p.top_k;
     }
     consumer_sync<kMrNC>();
-    stage_x<kMrCW, MAXB, kXRowList>(p.x, p.ldx, 0, kseg, nb, xs, xsum, xfac, red, 1, 1, 0, rowidx);
+    stage_x<kMrCW, MAXB, kXRowList>(p.x, p.ldx, 0, kseg, nb, xs, xfac, red, 1, 1, 0, rowidx);
     const int row = tid & (kMrRows - 1);
     const int h = tid >> 7;
-    const int xstride = xpad_len(kseg), sstride = kseg / 32;
+    const int xstride = xpad_len(kseg);
     float acc[MAXB];
 #pragma unroll
     for (int b = 0; b < MAXB; ++b) acc[b] = 0.f;
@@ -351,10 +350,9 @@ __device__ __forceinline__ bool moe_rows_group(const MoeRowsParams& p, const int
         const uint8_t* ub = smem + slot * R::stage_bytes + row * R::ub;
         const int hu = 2 * u + h;
         if constexpr (QT == 0)
-            dot_q8_0_half<MAXB>(ub + 136 * h, xs + hu * (kXPadEvery + kXPad), xstride, xsum + hu * 4, sstride, xfac,
-                                acc);
+            dot_q8_0_half<MAXB>(ub + 136 * h, xs + hu * (kXPadEvery + kXPad), xstride, xfac, acc);
         else
-            dot_q4_k_half<MAXB>(ub, h, xs + hu * (kXPadEvery + kXPad), xstride, xsum + hu * 4, sstride, xfac, acc);
+            dot_q4_k_half<MAXB>(ub, h, xs + hu * (kXPadEvery + kXPad), xstride, xfac, acc);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
     }
@@ -379,7 +377,7 @@ __device__ __forceinline__ bool moe_rows_group(const MoeRowsParams& p, const int
         const float out = NMAT == 2 ? silu_mul(a0, comb[(MAXB + b) * kMrRows + p.row_tile + r]) : a0;
         p.y[static_cast<int64_t>(pairs[b]) * p.ldy + n] = out;
     }
-    consumer_sync<kMrNC>();  // the next group overwrites xs, xsum and comb
+    consumer_sync<kMrNC>();  // the next group overwrites xs and comb
     return true;
 }
 
@@ -536,8 +534,6 @@ size_t moe_rows_layout(int qt, int64_t k, MoeRowsParams* p) {
     size_t off = ns * stage;
     p->xs_off = static_cast<uint32_t>(off);
     off += static_cast<size_t>(kMoeGroup) * xpad_len(kseg) * 4;
-    p->xsum_off = static_cast<uint32_t>(off);
-    off += static_cast<size_t>(kMoeGroup) * (kseg / 32) * 4;
     p->comb_off = static_cast<uint32_t>(off);
     off += 2 * static_cast<size_t>(kMoeGroup) * kMrRows * 4;
     off = (off + 15) & ~size_t{15};

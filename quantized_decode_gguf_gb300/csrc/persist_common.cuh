@@ -106,27 +106,24 @@ __device__ __forceinline__ bool wait_op_arrivals(unsigned* state, int op, unsign
 
 // Stage one activation vector of kseg floats for the register-resident
 // dot: one coalesced read pass (four values per lane and load group, up to 8
-// groups in flight per thread), raw values into xs (padded layout), 32-sums
-// into xsum, then scaled in place exactly as the launched GEMV's staging
-// does: x * r (RMSNorm) * 2^s. The source is a tagged vector (pairs carrying
+// groups in flight per thread), raw values into xs (padded layout), then
+// scaled in place exactly as the launched GEMV's staging does:
+// x * r (RMSNorm) * 2^s. The source is a tagged vector (pairs carrying
 // `tag`; pairs that are not yet current are re-read, bounded) or, for the
 // first layer, the caller's plain vector. XMODE: 0 plain, 1 RMSNorm, 2 gather
-// of the V heads, 3 plain with every `chunk` values scaled by their own
-// factor (applied as the values are read, before the sums and the scale). In the same pass threads t < nres read the next
+// of the V heads. In the same pass threads t < nres read the next
 // epilogue's residual, res_t[t] (tagged, `res_tag`) or res_p[t] (plain), into
 // res_dst[t]. Returns false on timeout or abort (all threads agree).
 // What stage_vec needs besides the source: the workspace state (for the
-// bounded waits), the head layout (XMODE 2) and the chunk scales (XMODE 3).
+// bounded waits) and the head layout (XMODE 2).
 struct StageCtx {
     unsigned* state;
     int n_q, n_kv, head_dim;
-    const float* scale;  // XMODE 3: x[k] = scale[k / chunk] * src[k]
-    int chunk;
 };
 
 template <int XMODE>
 __device__ __forceinline__ bool stage_vec(const StageCtx& p, const uint2* src_t, const float* src_p, unsigned tag,
-                                          int kseg, float* xs, float* xsum, float* xfac, float* red, int* flag,
+                                          int kseg, float* xs, float* xfac, float* red, int* flag,
                                           const uint2* res_t, const float* res_p, unsigned res_tag, float* res_dst,
                                           int nres, int* retries, int trace_op) {
     (void)trace_op;
@@ -185,38 +182,19 @@ __device__ __forceinline__ bool stage_vec(const StageCtx& p, const uint2* src_t,
                         miss &= ~(1u << i);
             }
         }
-        if constexpr (XMODE == 3) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int c = base + i * kNC + tid;
-                if (c < nsrc4) {
-                    const float f = p.scale[(4 * c) / p.chunk];
-                    v[i].x *= f;
-                    v[i].y *= f;
-                    v[i].z *= f;
-                    v[i].w *= f;
-                }
-            }
-        }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int c = base + i * kNC + tid;
             if (base + i * kNC >= nsrc4) break;  // uniform over the CTA
-            float cs = (v[i].x + v[i].y) + (v[i].z + v[i].w);
-            cs += __shfl_xor_sync(0xFFFFFFFFu, cs, 1);
-            cs += __shfl_xor_sync(0xFFFFFFFFu, cs, 2);
-            cs += __shfl_xor_sync(0xFFFFFFFFu, cs, 4);
             if (c < nsrc4) {
                 if constexpr (XMODE == 2) {
                     const int e = 4 * c, g = e / p.head_dim, o = e - g * p.head_dim;
                     for (int m = 0; m < group; ++m) {
                         const int k = (g * group + m) * p.head_dim + o;
                         *reinterpret_cast<float4*>(xs + xpad_idx(k)) = v[i];
-                        if ((lane & 7) == 0) xsum[k >> 5] = cs;
                     }
                 } else {
                     *reinterpret_cast<float4*>(xs + xpad_idx(4 * c)) = v[i];
-                    if ((lane & 7) == 0) xsum[c >> 3] = cs;
                 }
                 mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
                 if constexpr (XMODE == 1) {
@@ -270,7 +248,7 @@ __device__ __forceinline__ bool stage_vec(const StageCtx& p, const uint2* src_t,
     const int se = pick_scale_exp(m * r);
     const int e1 = min(se, 127);
     const float f1 = __int_as_float((e1 + 127) << 23), f2 = __int_as_float((se - e1 + 127) << 23);
-    if (tid == 0) xfac[0] = __int_as_float((149 - se + 127) << 23);
+    if (tid == 0) xfac[0] = __int_as_float((kWShift - se + 127) << 23);
     const bool all_ok = *flag == 0;
     for (int k4 = tid; k4 < n4; k4 += kNC) {
         float4* q = reinterpret_cast<float4*>(xs + xpad_idx(4 * k4));
@@ -286,9 +264,6 @@ __device__ __forceinline__ bool stage_vec(const StageCtx& p, const uint2* src_t,
         v.z = v.z * f1 * f2;
         v.w = v.w * f1 * f2;
         *q = v;
-    }
-    if constexpr (XMODE == 1) {
-        for (int i = tid; i < kseg / 32; i += kNC) xsum[i] *= r;
     }
     consumer_sync<kNC>();
     return all_ok;
@@ -317,8 +292,7 @@ __device__ __forceinline__ bool stage_wait(uint64_t* bar, uint32_t parity) {
 // false on a wait timeout.
 template <int QT, int NMAT, int NS, class EpiF>
 __device__ __forceinline__ bool consume_xr(const Tile& t, int segs, const uint8_t* stages, uint64_t* full,
-                                           uint64_t* empty, int& s, const float (&xr)[kHalfK], const float (&xsr)[4],
-                                           float xfac, float* part, float* rsum, bool compute, int trace_op,
+                                           uint64_t* empty, int& s, const float (&xr)[kHalfK], float xfac, float* part, float* rsum, bool compute, int trace_op,
                                            EpiF epi) {
     (void)trace_op;
     using C = KCfg<QT, kCW, NS>;
@@ -339,9 +313,9 @@ __device__ __forceinline__ bool consume_xr(const Tile& t, int segs, const uint8_
             const uint8_t* ub = stages + slot * C::stage_bytes + (j * t.useg + (pos >> 1)) * C::ub;
             float acc;
             if constexpr (QT == 0)
-                acc = dot_q8_0_half_xr(ub + 136 * (pos & 1), xr, xsr, xfac);
+                acc = dot_q8_0_half_xr(ub + 136 * (pos & 1), xr, xfac);
             else
-                acc = dot_q4_k_half_xr(ub, pos & 1, xr, xsr, xfac);
+                acc = dot_q4_k_half_xr(ub, pos & 1, xr, xfac);
             part[seg * seg_half + pos] = acc;
         }
         __syncwarp();
