@@ -275,16 +275,19 @@ def moe_route(logits: np.ndarray, top_k: int):
     return idx, p
 
 
-def moe_ffn(wg: np.ndarray, wu: np.ndarray, wd: np.ndarray, x: np.ndarray, logits: np.ndarray,
-            top_k: int, eps: float = 1e-3, p_rel_err: float = 1e-5):
+def moe_ffn(wg, wu, wd, x: np.ndarray, logits: np.ndarray,
+            top_k: int, eps: float = 1e-3, p_rel_err: float = 1e-5, sum_rel_err: float = 1e-6):
     """Routed expert FFN: y_t = sum_k p_{t,k} FFN_{e_{t,k}}(x_t).
 
-    ``wg``, ``wu``: fp32 [E, d_ff, d_model]; ``wd``: fp32 [E, d_model, d_ff];
-    ``x``: [T, d_model]; ``logits``: [T, E]. Returns (y, tol, idx, p).
+    ``wg``, ``wu``: fp32 [E, d_ff, d_model]; ``wd``: fp32 [E, d_model, d_ff]
+    (or any mapping from expert index to that expert's matrix, so that only
+    the routed experts need dequantising); ``x``: [T, d_model]; ``logits``:
+    [T, E]. Returns (y, tol, idx, p).
 
-    ``tol`` = sum_k p_k (tol_k + p_rel_err |FFN_k(x_t)|) + eps_c sum_k p_k |FFN_k|,
+    ``tol`` = sum_k p_k (tol_k + p_rel_err |FFN_k(x_t)| + sum_rel_err |FFN_k(x_t)|),
     covering each expert's FFN bound, a relative error of ``p_rel_err`` in
-    each routing weight (fp32 exp and divide) and the fp32 weighted sum.
+    each routing weight (fp32 exp and divide) and ``sum_rel_err`` for the
+    fp32 weighted sum of at most a few dozen terms.
     """
     x = np.atleast_2d(np.asarray(x, dtype=np.float64))
     idx, p = moe_route(logits, top_k)
@@ -296,7 +299,7 @@ def moe_ffn(wg: np.ndarray, wu: np.ndarray, wd: np.ndarray, x: np.ndarray, logit
             e = int(idx[t, j])
             ye, te, _ = swiglu_ffn(wg[e], wu[e], wd[e], x[t:t + 1], eps)
             y[t] += p[t, j] * ye[0]
-            tol[t] += p[t, j] * (te[0] + p_rel_err * np.abs(ye[0]) + 1e-6 * np.abs(ye[0]))
+            tol[t] += p[t, j] * (te[0] + (p_rel_err + sum_rel_err) * np.abs(ye[0]))
     return y, tol, idx, p
 
 

@@ -105,19 +105,12 @@ def test_moe_ffn_within_bound(qtype, t, e, k, d_model, d_ff):
     ridx, rp = oracle.moe_route(logits, k)
     assert np.array_equal(idx, ridx), "routing differs from the oracle"
     assert np.allclose(p, rp, rtol=1e-6, atol=0)
-    # expert FFNs only for the routed experts (dequantise what is used)
+    # the oracle's MoE block and bound; only the routed experts are dequantised
     used = sorted(set(ridx.ravel().tolist()))
     dg = {i: oracle.dequant(qtype, wg[i], d_ff, d_model) for i in used}
     du = {i: oracle.dequant(qtype, wu[i], d_ff, d_model) for i in used}
     dd = {i: oracle.dequant(qtype, wd[i], d_model, d_ff) for i in used}
-    ref = np.zeros((t, d_model))
-    tol = np.zeros((t, d_model))
-    for ti in range(t):
-        for j in range(k):
-            ex = int(ridx[ti, j])
-            ye, te, _ = oracle.swiglu_ffn(dg[ex], du[ex], dd[ex], x[ti:ti + 1])
-            ref[ti] += rp[ti, j] * ye[0]
-            tol[ti] += rp[ti, j] * (te[0] + 1e-5 * np.abs(ye[0]) + 1e-6 * np.abs(ye[0]))
+    ref, tol, _, _ = oracle.moe_ffn(dg, du, dd, x, logits, k)
     assert_within(y, ref, tol, f"moe {qtype} T={t} E={e} k={k}")
     check_device_clean()
 
