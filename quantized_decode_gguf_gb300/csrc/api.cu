@@ -189,6 +189,19 @@ phb_status set_last_error(phb_status s, const char* fmt, ...) {
     g_last_error = buf;
     return s;
 }
+// Host-side argument checks of the SwiGLU block (pointers, alignment,
+// shapes); touches no device.
+phb_status validate_ffn(int qtype, const void* Wgate, const void* Wup, const void* Wdown, const float* X,
+                        const float* Y, int64_t d_model, int64_t d_ff, int batch) {
+    const int qt = qt_of(qtype);
+    phb_status st = validate_gemv(qt, Wgate, X, Y, d_ff, d_model, batch);
+    if (st != PHB_OK) return st;
+    PHB_REQUIRE(Wup && Wdown, PHB_ERR_INVALID_ARG, "null weight pointer");
+    PHB_REQUIRE(aligned16(Wup) && aligned16(Wdown), PHB_ERR_ALIGN, "pointers must be 16-byte aligned");
+    PHB_REQUIRE(d_ff % block_weights(qt) == 0, PHB_ERR_SHAPE, "%s needs d_ff %% %lld == 0", qt_name(qt),
+                static_cast<long long>(block_weights(qt)));
+    return PHB_OK;
+}
 }  // namespace phb
 
 extern "C" {
@@ -296,12 +309,9 @@ size_t phb_ffn_swiglu_workspace_size(int qtype, int64_t d_model, int64_t d_ff, i
 phb_status phb_ffn_swiglu(int qtype, const void* Wgate, const void* Wup, const void* Wdown, const float* X, float* Y,
                           int64_t d_model, int64_t d_ff, int batch, void* ws, size_t ws_bytes, phb_stream_t stream) {
     const int qt = qt_of(qtype);
-    phb_status st = validate_gemv(qt, Wgate, X, Y, d_ff, d_model, batch);
+    phb_status st = phb::validate_ffn(qtype, Wgate, Wup, Wdown, X, Y, d_model, d_ff, batch);
     if (st != PHB_OK) return st;
-    PHB_REQUIRE(Wup && Wdown, PHB_ERR_INVALID_ARG, "null weight pointer");
-    PHB_REQUIRE(aligned16(Wup) && aligned16(Wdown) && aligned16(ws), PHB_ERR_ALIGN, "pointers must be 16-byte aligned");
-    PHB_REQUIRE(d_ff % block_weights(qt) == 0, PHB_ERR_SHAPE, "%s needs d_ff %% %lld == 0", qt_name(qt),
-                static_cast<long long>(block_weights(qt)));
+    PHB_REQUIRE(aligned16(ws), PHB_ERR_ALIGN, "pointers must be 16-byte aligned");
     const FfnWs need = ffn_ws(qt, d_model, d_ff, batch, nullptr);
     PHB_REQUIRE(ws && ws_bytes >= need.bytes, PHB_ERR_WORKSPACE, "workspace needs %zu bytes (got %zu)", need.bytes,
                 ws_bytes);

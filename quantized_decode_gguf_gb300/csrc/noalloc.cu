@@ -30,9 +30,10 @@ extern "C" size_t phb_ffn_swiglu_noalloc_max_scratch(void) { return kNoAllocScra
 extern "C" phb_status phb_ffn_swiglu_noalloc(int qtype, const void* Wgate, const void* Wup, const void* Wdown,
                                              const float* X, float* Y, int64_t d_model, int64_t d_ff, int batch,
                                              phb_stream_t stream) {
+    // Bad arguments fail here, before anything touches a device.
+    const phb_status st = phb::validate_ffn(qtype, Wgate, Wup, Wdown, X, Y, d_model, d_ff, batch);
+    if (st != PHB_OK) return st;
     const size_t need = phb_ffn_swiglu_workspace_size(qtype, d_model, d_ff, batch);
-    // An invalid shape has no workspace size: phb_ffn_swiglu reports which argument is wrong.
-    if (need == 0) return phb_ffn_swiglu(qtype, Wgate, Wup, Wdown, X, Y, d_model, d_ff, batch, nullptr, 0, stream);
     if (need > kNoAllocScratchBytes)
         return phb::set_last_error(PHB_ERR_WORKSPACE,
                                    "phb_ffn_swiglu_noalloc: this shape needs %zu bytes of scratch; the static "

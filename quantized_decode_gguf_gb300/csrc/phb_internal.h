@@ -12,6 +12,8 @@ namespace phb {
 
 // Record the message of a failed call for phb_last_error() and return `s`.
 phb_status set_last_error(phb_status s, const char* fmt, ...);
+phb_status validate_ffn(int qtype, const void* Wgate, const void* Wup, const void* Wdown, const float* X,
+                        const float* Y, int64_t d_model, int64_t d_ff, int batch);
 
 // ---------------------------------------------------------------- device info
 int device_sm_count();         // multiprocessors of the current device (cached)

@@ -140,3 +140,13 @@ def test_attention_binding_rejects_a_non_fp16_cache():
         phb.attention_decode(q, k32, k32.half(), 16, 8, 2, 64)
     with pytest.raises(TypeError):
         phb.attention_decode(q, k32.half(), k32, 16, 8, 2, 64)
+
+
+def test_ffn_noalloc_rejects_bad_arguments_without_a_device(lib):
+    # argument errors come back before the device is looked up (no GPU here)
+    f = lib.phb_ffn_swiglu_noalloc
+    assert f(8, FAKE, None, FAKE, FAKE, FAKE, 2048, 768, 1, None) == INVALID
+    assert f(8, FAKE, FAKE + 4, FAKE, FAKE, FAKE, 2048, 768, 1, None) == ALIGN
+    assert f(12, FAKE, FAKE, FAKE, FAKE, FAKE, 2048, 768 + 32, 1, None) == SHAPE
+    assert f(8, FAKE, FAKE, FAKE, FAKE, FAKE, 2048, 768, 0, None) == INVALID
+    assert f(12, FAKE, FAKE, FAKE, FAKE, FAKE, 8192, 28672, 8, None) == WORKSPACE and "scratch" in _err(lib)
