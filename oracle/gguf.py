@@ -232,6 +232,20 @@ def silu(g: np.ndarray) -> np.ndarray:
 SILU_SLOPE_MAX = 1.1  # max |d silu / dg| = 1.0998..., rounded up
 
 
+def _swiglu_bound(g, dg, u, du, eps: float):
+    """h = silu(g) * u and a bound of |h~ - h|.
+
+    Given |g~ - g| <= dg, |u~ - u| <= du and an fp32 evaluation of silu and
+    the product with relative error at most ``eps``: by the mean value
+    theorem |silu(g~) - silu(g)| <= 1.1 dg, so
+        d1 = 1.1 dg (|u| + du) + |silu(g)| du,   dh = d1 + eps (|h| + d1).
+    """
+    sg = silu(g)
+    h = sg * u
+    d1 = SILU_SLOPE_MAX * dg * (np.abs(u) + du) + np.abs(sg) * du
+    return h, d1 + eps * (np.abs(h) + d1)
+
+
 def swiglu_ffn(wg: np.ndarray, wu: np.ndarray, wd: np.ndarray, x: np.ndarray, eps: float = 1e-3):
     """SwiGLU feed-forward block and its error bound.
 
@@ -239,21 +253,37 @@ def swiglu_ffn(wg: np.ndarray, wu: np.ndarray, wd: np.ndarray, x: np.ndarray, ep
     [B, d_model]. Returns (y [B, d_model], tol [B, d_model], h [B, d_ff]).
 
     ``tol`` propagates the per-GEMV contract |err| <= eps * sum|w x| through
-    the block: with g, u the gate and up outputs and S_g, S_u their sums of
-    absolute terms, the error of h_j = silu(g_j) u_j is at most
-        dh_j = 1.1 eps S_g,j (|u_j| + eps S_u,j) + |silu(g_j)| eps S_u,j + eps |h_j|
-    (1.1 bounds |silu'|; the last term covers the fp32 evaluation of silu and
-    the product), and the output error is at most
-        eps * sum_j |wd_ij h_j| + sum_j |wd_ij| dh_j.
+    the block: the gate and up outputs g, u carry at most eps * S_g and
+    eps * S_u, the activation h = silu(g) u then at most dh (see
+    :func:`_swiglu_bound`), and the down projection, whose contract applies
+    to the activation it is actually given, at most
+        eps * sum_j |wd_ij h_j| + (1 + eps) * sum_j |wd_ij| dh_j.
+    This bound is valid but grows with sum_j |wd_ij| / |y_i|; for checking a
+    device against it stage by stage see :func:`swiglu_stages`.
     """
     g, sg = gemv(wg, x)
     u, su = gemv(wu, x)
-    sg_u = silu(g)
-    h = sg_u * u
-    dh = SILU_SLOPE_MAX * eps * sg * (np.abs(u) + eps * su) + np.abs(sg_u) * eps * su + eps * np.abs(h)
-    y, sd = gemv(wd, h)
-    tol = eps * sd + dh @ np.abs(np.asarray(wd, dtype=np.float64)).T
+    h, dh = _swiglu_bound(g, eps * sg, u, eps * su, eps)
+    y, tol = _gemv_bound(wd, h, dh, eps)
     return y, tol, h
+
+
+def swiglu_stages(wg: np.ndarray, wu: np.ndarray, wd: np.ndarray, x: np.ndarray, h_dev: np.ndarray,
+                  eps: float = 1e-3):
+    """The SwiGLU block checked one stage at a time.
+
+    ``h_dev`` is the activation a device computed ([B, d_ff]). Returns
+    ((h, h_tol), (y, y_tol)): the activation and its bound from ``x`` (the
+    gate/up contract and the elementwise step, as in :func:`swiglu_ffn`), and
+    y = wd h_dev with the GEMV contract eps * sum|wd h_dev| for the input the
+    device actually used. Each stage is one GEMV deep, so neither bound
+    compounds.
+    """
+    g, sg = gemv(wg, x)
+    u, su = gemv(wu, x)
+    h, dh = _swiglu_bound(g, eps * sg, u, eps * su, eps)
+    y, s = gemv(wd, h_dev)
+    return (h, dh), (y, eps * s)
 
 
 # ----------------------------------------------------------------------------
@@ -284,10 +314,11 @@ def moe_ffn(wg, wu, wd, x: np.ndarray, logits: np.ndarray,
     the routed experts need dequantising); ``x``: [T, d_model]; ``logits``:
     [T, E]. Returns (y, tol, idx, p).
 
-    ``tol`` = sum_k p_k (tol_k + p_rel_err |FFN_k(x_t)| + sum_rel_err |FFN_k(x_t)|),
-    covering each expert's FFN bound, a relative error of ``p_rel_err`` in
-    each routing weight (fp32 exp and divide) and ``sum_rel_err`` for the
-    fp32 weighted sum of at most a few dozen terms.
+    ``tol`` = sum_k p_k (tol_k + c (|FFN_k(x_t)| + tol_k)), c = a + b + a b,
+    covering each expert's FFN bound, a relative error of at most
+    a = ``p_rel_err`` in each routing weight (fp32 exp and divide) and
+    b = ``sum_rel_err`` for the fp32 weighted sum of at most a few dozen
+    terms (each applied to the expert output the device actually has).
     """
     x = np.atleast_2d(np.asarray(x, dtype=np.float64))
     idx, p = moe_route(logits, top_k)
@@ -299,8 +330,43 @@ def moe_ffn(wg, wu, wd, x: np.ndarray, logits: np.ndarray,
             e = int(idx[t, j])
             ye, te, _ = swiglu_ffn(wg[e], wu[e], wd[e], x[t:t + 1], eps)
             y[t] += p[t, j] * ye[0]
-            tol[t] += p[t, j] * (te[0] + (p_rel_err + sum_rel_err) * np.abs(ye[0]))
+            c = p_rel_err + sum_rel_err + p_rel_err * sum_rel_err
+            tol[t] += p[t, j] * (te[0] + c * (np.abs(ye[0]) + te[0]))
     return y, tol, idx, p
+
+
+def moe_stages(wg, wu, wd, x: np.ndarray, logits: np.ndarray, top_k: int, h_dev: np.ndarray, y_pair_dev: np.ndarray,
+               eps: float = 1e-3, p_rel_err: float = 1e-5, sum_rel_err: float = 1e-6):
+    """The routed expert FFN checked one stage at a time.
+
+    ``h_dev`` [T * top_k, d_ff] and ``y_pair_dev`` [T * top_k, d_model] are a
+    device's per-(token, slot) activations and expert outputs (pair
+    t * top_k + k, slots in descending logit order). Returns
+    (idx, p, (h, h_tol), (yp, yp_tol), (y, y_tol)):
+      * h, h_tol: each pair's activation and bound from x_t (:func:`swiglu_stages`);
+      * yp, yp_tol: each pair's down projection of h_dev and its contract;
+      * y, y_tol: the combine sum_k p_k y_pair_dev with the routing-weight and
+        weighted-sum errors of :func:`moe_ffn`.
+    ``wg``, ``wu``, ``wd`` may be mappings from expert index to matrix.
+    """
+    x = np.atleast_2d(np.asarray(x, dtype=np.float64))
+    idx, p = moe_route(logits, top_k)
+    t_count = x.shape[0]
+    hs, dhs, yps, dyps = [], [], [], []
+    for t in range(t_count):
+        for j in range(top_k):
+            e = int(idx[t, j])
+            pair = t * top_k + j
+            (h, dh), (yp, dyp) = swiglu_stages(wg[e], wu[e], wd[e], x[t:t + 1], h_dev[pair:pair + 1], eps)
+            hs.append(h[0])
+            dhs.append(dh[0])
+            yps.append(yp[0])
+            dyps.append(dyp[0])
+    ypd = np.asarray(y_pair_dev, dtype=np.float64).reshape(t_count, top_k, -1)
+    y = np.einsum("tk,tkd->td", p, ypd)
+    c = p_rel_err + sum_rel_err + p_rel_err * sum_rel_err
+    y_tol = c * np.einsum("tk,tkd->td", p, np.abs(ypd))
+    return idx, p, (np.array(hs), np.array(dhs)), (np.array(yps), np.array(dyps)), (y, y_tol)
 
 
 # ----------------------------------------------------------------------------
@@ -377,23 +443,54 @@ def attention_decode(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, n_
 
 
 def _rmsnorm_bound(x: np.ndarray, dx: np.ndarray, eps_norm: float, eps: float = RMS_EPS):
-    """First-order bound of |rmsnorm(x~) - rmsnorm(x)| given |x~ - x| <= dx.
+    """Bound of |h~ - rmsnorm(x)| for h~ = x~ r~ (1 + t2), with |x~ - x| <= dx,
+    r~ = r(x~) (1 + t1) and |t1|, |t2| <= eps_norm (the fp32 evaluation).
 
-    With r = (mean x^2 + eps)^-1/2: dr <= r^3 * sum|x_i| dx_i / n + eps_norm r,
-    and dh_i <= r dx_i + |x_i| dr + eps_norm |h_i|.
+    With m = mean x^2 and r = (m + eps)^-1/2: |mean x~^2 - m| <= dm =
+    (2 sum|x| dx + sum dx^2) / n, and |dr/dm| = r^3 / 2 is largest at the
+    smallest m, so |r(x~) - r(x)| <= dr_in = dm / 2 (m + eps - dm)^-3/2
+    (infinite when dm >= m + eps). Then dr = dr_in + eps_norm (r + dr_in)
+    bounds |r~ - r|, and
+        |h~ - h| <= (1 + eps_norm) ((r + dr) dx + |x| dr) + eps_norm |h|.
     """
+    x = np.asarray(x, dtype=np.float64)
+    dx = np.asarray(dx, dtype=np.float64)
     n = x.shape[-1]
-    r = 1.0 / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
-    dr = r ** 3 * np.sum(np.abs(x) * dx, axis=-1, keepdims=True) / n + eps_norm * r
-    h = x * r
-    return r * dx + np.abs(x) * dr + eps_norm * np.abs(h)
+    m = np.mean(x * x, axis=-1, keepdims=True)
+    r = 1.0 / np.sqrt(m + eps)
+    dm = (2.0 * np.sum(np.abs(x) * dx, axis=-1, keepdims=True) + np.sum(dx * dx, axis=-1, keepdims=True)) / n
+    lo = m + eps - dm
+    with np.errstate(divide="ignore", invalid="ignore"):
+        dr_in = np.where(lo > 0, 0.5 * dm * np.abs(lo) ** -1.5, np.inf)
+    dr = dr_in + eps_norm * (r + dr_in)
+    with np.errstate(invalid="ignore"):
+        dh = (1.0 + eps_norm) * ((r + dr) * dx + np.abs(x) * dr) + eps_norm * np.abs(x * r)
+    return np.where(np.isfinite(dr), dh, np.inf)
+
+
+def _abs_matvec(dx: np.ndarray, aw: np.ndarray) -> np.ndarray:
+    """dx @ aw.T for nonnegative dx and aw, where an infinite dx_j makes every
+    output with a nonzero weight in column j infinite (never NaN)."""
+    fin = np.isfinite(dx)
+    out = np.where(fin, dx, 0.0) @ aw.T
+    hit = (~fin).astype(np.float64) @ (aw.T > 0).astype(np.float64)
+    return np.where(hit > 0, np.inf, out)
 
 
 def _gemv_bound(w: np.ndarray, x: np.ndarray, dx: np.ndarray, eps: float):
-    """y = w x and its bound eps * sum|w x| + sum|w| dx (plus the input's own error)."""
+    """y = w x and its bound eps * sum|w x| + (1 + eps) sum|w| dx.
+
+    The contract applies to the input the device actually has, x~ with
+    |x~ - x| <= dx: |y~ - y| <= eps sum|w x~| + sum|w| dx, and
+    sum|w x~| <= sum|w x| + sum|w| dx.
+    """
     y, s = gemv(w, x)
     aw = np.abs(np.asarray(w, dtype=np.float64))
-    return y, eps * s + eps * (dx @ aw.T) + dx @ aw.T
+    wdx = _abs_matvec(np.asarray(dx, dtype=np.float64), aw)
+    return y, eps * s + (1.0 + eps) * wdx
+
+
+ADD_REL = 1e-7  # >= 2^-24: one fp32 rounding of a residual add, relative to the rounded sum's magnitude
 
 
 def decode_layer(x: np.ndarray, dx: np.ndarray, w_qkv, w_o, w_gate, w_up, w_down,
@@ -404,6 +501,11 @@ def decode_layer(x: np.ndarray, dx: np.ndarray, w_qkv, w_o, w_gate, w_up, w_down
     x1 = x + W_o attn(W_qkv rmsnorm(x)); x2 = x1 + W_down (silu(W_gate h) * (W_up h)),
     h = rmsnorm(x1). All weights fp32 dequantised [out, in]. ``dx`` bounds
     the error already in ``x`` (zeros for an exact input). Returns (x2, dx2).
+
+    The bound chains the per-GEMV contract through four GEMVs with the
+    triangle inequality; it is valid, but each GEMV multiplies the incoming
+    allowance by its row sums of |w|, so at model sizes it dwarfs the output.
+    A device is checked against :func:`decode_layer_stages` instead.
     """
     x = np.atleast_2d(np.asarray(x, dtype=np.float64))
     dx = np.atleast_2d(np.asarray(dx, dtype=np.float64))
@@ -414,15 +516,47 @@ def decode_layer(x: np.ndarray, dx: np.ndarray, w_qkv, w_o, w_gate, w_up, w_down
     da = attention_pos0(dqkv, n_q_heads, n_kv_heads, head_dim)
     o, do = _gemv_bound(w_o, a, da, eps)
     x1 = x + o
-    dx1 = dx + do + 1e-7 * np.abs(x1)
+    dx1 = dx + do + ADD_REL * (np.abs(x1) + dx + do)
     h2 = rmsnorm(x1)
     dh2 = _rmsnorm_bound(x1, dx1, eps_norm)
     g, dg = _gemv_bound(w_gate, h2, dh2, eps)
     u, du = _gemv_bound(w_up, h2, dh2, eps)
-    sg = silu(g)
-    act = sg * u
-    dact = SILU_SLOPE_MAX * dg * (np.abs(u) + du) + np.abs(sg) * du + eps * np.abs(act)
+    act, dact = _swiglu_bound(g, dg, u, du, eps)
     f, df = _gemv_bound(w_down, act, dact, eps)
     x2 = x1 + f
-    dx2 = dx1 + df + 1e-7 * np.abs(x2)
+    dx2 = dx1 + df + ADD_REL * (np.abs(x2) + dx1 + df)
     return x2, dx2
+
+
+def decode_layer_stages(x: np.ndarray, qkv_dev: np.ndarray, x1_dev: np.ndarray, act_dev: np.ndarray,
+                        w_qkv, w_o, w_gate, w_up, w_down, n_q_heads: int, n_kv_heads: int, head_dim: int,
+                        eps: float = 1e-3, eps_norm: float = 1e-5):
+    """One decoder layer checked one stage at a time, from the intermediate
+    vectors a device computed (its QKV vector, its x1 = x + W_o attn, its
+    SwiGLU activation; each [1, n]).
+
+    Returns {"qkv": (ref, tol), "x1": ..., "act": ..., "out": ...}, each
+    stage's reference and bound computed from the device's own input to
+    that stage, one GEMV deep:
+      qkv: W_qkv rmsnorm(x), with rmsnorm's evaluation error;
+      x1:  x + W_o attn(qkv_dev), the contract plus the residual add's rounding;
+      act: silu(W_gate h2) * (W_up h2), h2 = rmsnorm(x1_dev) (:func:`_swiglu_bound`);
+      out: x1_dev + W_down act_dev, the contract plus the residual add's rounding.
+    """
+    x = np.atleast_2d(np.asarray(x, dtype=np.float64))
+    qkv_dev, x1_dev, act_dev = (np.atleast_2d(np.asarray(v, dtype=np.float64)) for v in (qkv_dev, x1_dev, act_dev))
+    out = {}
+    h = rmsnorm(x)
+    out["qkv"] = _gemv_bound(w_qkv, h, _rmsnorm_bound(x, np.zeros_like(x), eps_norm), eps)
+    o, so = gemv(w_o, attention_pos0(qkv_dev, n_q_heads, n_kv_heads, head_dim))
+    x1 = x + o
+    out["x1"] = (x1, eps * so + ADD_REL * (np.abs(x1) + eps * so))
+    h2 = rmsnorm(x1_dev)
+    dh2 = _rmsnorm_bound(x1_dev, np.zeros_like(x1_dev), eps_norm)
+    g, dg = _gemv_bound(w_gate, h2, dh2, eps)
+    u, du = _gemv_bound(w_up, h2, dh2, eps)
+    out["act"] = _swiglu_bound(g, dg, u, du, eps)
+    f, sf = gemv(w_down, act_dev)
+    x2 = x1_dev + f
+    out["out"] = (x2, eps * sf + ADD_REL * (np.abs(x2) + eps * sf))
+    return out
