@@ -125,7 +125,9 @@ phb_status phb_gemv_q4_k(const void* W, const float* X, float* Y, int64_t n, int
  * Wgate, Wup: [d_ff][d_model]; Wdown: [d_model][d_ff] (all qtype);
  * X: [batch][d_model]; Y: [batch][d_model]; batch 1..8. d_model and d_ff must
  * be multiples of the block size (256 for Q4_K, 32 for Q8_0). The hidden
- * activation h lives in ws.
+ * activation h lives in ws: once the call has run (stream order), ws
+ * begins with h as [batch][d_ff] fp32, so a checker can verify the down
+ * projection from the activation the GPU actually used.
  * ------------------------------------------------------------------------- */
 size_t phb_ffn_swiglu_workspace_size(int qtype, int64_t d_model, int64_t d_ff, int batch);
 phb_status phb_ffn_swiglu(int qtype, const void* Wgate, const void* Wup, const void* Wdown,
@@ -151,6 +153,11 @@ phb_status phb_ffn_swiglu(int qtype, const void* Wgate, const void* Wup, const v
  * the same, otherwise untouched, workspace to later calls (each call returns
  * the counters to zero); calls sharing a workspace must not overlap on the
  * GPU. After a device error (phb_device_error) zero it again.
+ * Once the call has run (stream order), ws begins with the per-pair expert
+ * outputs FFN_{e_{t,k}}(X[t]) as [n_tokens * top_k][d_model] fp32 (pair
+ * t * top_k + k), followed, at the next multiple of 256 bytes, by their
+ * SwiGLU activations [n_tokens * top_k][d_ff], so that each stage can be
+ * checked from the values the GPU actually used.
  * ------------------------------------------------------------------------- */
 size_t phb_moe_ffn_workspace_size(int qtype, int64_t n_tokens, int64_t d_model, int64_t d_ff,
                                   int n_experts, int top_k);
@@ -224,6 +231,25 @@ phb_status phb_decode_step_unfused(int qtype, const phb_dense_layer* layers, int
                                    int64_t d_model, int n_q_heads, int n_kv_heads, int head_dim, int64_t d_ff,
                                    const float* x_in, float* x_out,
                                    void* ws, size_t ws_bytes, phb_stream_t stream);
+
+/* Checking aid for the decode step (the README's examples check the decode
+ * path from its intermediate values: `fuse_check` compares the fused and
+ * the launched decode, `kv_check` one decode step against a recompute).
+ * Copies, in stream order, the intermediate vectors of the LAST layer of
+ * the most recent decode-step call that used `ws` (fused != 0: a
+ * phb_decode_step call; fused == 0: a phb_decode_step_unfused call) into
+ * caller-owned device buffers:
+ *   qkv [(n_q_heads + 2*n_kv_heads) * head_dim]  Wqkv . rmsnorm(x)
+ *   x1  [d_model]                                 x + Wo . attention
+ *   act [d_ff]                                    silu(Wgate.h) * (Wup.h)
+ * so that each GEMV of the layer can be checked from the input the GPU
+ * actually used. The shape arguments must be those of that call; ws is not
+ * modified. Errors: PHB_ERR_INVALID_ARG (null pointer, size <= 0),
+ * PHB_ERR_SHAPE (sizes beyond the decode step's limits), PHB_ERR_ALIGN
+ * (ws not 16-byte aligned), PHB_ERR_CUDA. */
+phb_status phb_decode_step_probe(int fused, int64_t d_model, int n_q_heads, int n_kv_heads, int head_dim,
+                                 int64_t d_ff, const void* ws, float* qkv, float* x1, float* act,
+                                 phb_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Decode attention at context depth (Phobos README: `phobos-bench -d N`,

@@ -46,6 +46,8 @@ SIGNATURES = {
                                  _c_sz, _c_vp]),
     "phb_decode_step_unfused": (_c_int, [_c_int, _c_vp, _c_int, _c_i64, _c_int, _c_int, _c_int, _c_i64, _c_vp, _c_vp,
                                          _c_vp, _c_sz, _c_vp]),
+    "phb_decode_step_probe": (_c_int, [_c_int, _c_i64, _c_int, _c_int, _c_int, _c_i64, _c_vp, _c_vp, _c_vp, _c_vp,
+                                       _c_vp]),
     "phb_attention_decode_workspace_size": (_c_sz, [_c_i64, _c_int, _c_int, _c_int]),
     "phb_attention_decode": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_i64, _c_int, _c_int, _c_int, ctypes.c_float,
                                       _c_vp, _c_sz, _c_vp]),

@@ -215,6 +215,17 @@ def decode_step(qtype, table, n_layers: int, d_model: int, n_q: int, n_kv: int, 
     return x_out
 
 
+def decode_step_probe(ws: torch.Tensor, d_model: int, n_q: int, n_kv: int, head_dim: int, d_ff: int,
+                      fused: bool = True):
+    """phb_decode_step_probe: (qkv, x1, act) of the last layer of the latest decode step through ``ws``."""
+    qkv = torch.empty((n_q + 2 * n_kv) * head_dim, dtype=torch.float32, device=ws.device)
+    x1 = torch.empty(d_model, dtype=torch.float32, device=ws.device)
+    act = torch.empty(d_ff, dtype=torch.float32, device=ws.device)
+    _check(_lib.load().phb_decode_step_probe(int(bool(fused)), d_model, n_q, n_kv, head_dim, d_ff, _ptr(ws),
+                                             _ptr(qkv), _ptr(x1), _ptr(act), _stream()))
+    return qkv, x1, act
+
+
 # ---------------------------------------------------------------- decode attention
 
 def attention_workspace_size(n_ctx: int, n_q: int, n_kv: int, head_dim: int) -> int:

@@ -575,6 +575,32 @@ phb_status phb_decode_step_unfused(int qtype, const phb_dense_layer* layers, int
     return ok();
 }
 
+phb_status phb_decode_step_probe(int fused, int64_t d_model, int n_q_heads, int n_kv_heads, int head_dim,
+                                 int64_t d_ff, const void* ws, float* qkv, float* x1, float* act,
+                                 phb_stream_t stream) {
+    PHB_REQUIRE(ws && qkv && x1 && act, PHB_ERR_INVALID_ARG, "null pointer");
+    PHB_REQUIRE(d_model > 0 && n_q_heads > 0 && n_kv_heads > 0 && head_dim > 0 && d_ff > 0, PHB_ERR_INVALID_ARG,
+                "sizes must be positive");
+    PHB_REQUIRE(d_model <= 16384 && d_ff <= 16384 && static_cast<int64_t>(n_q_heads + 2 * n_kv_heads) * head_dim <= 65536,
+                PHB_ERR_SHAPE, "decode step sizes out of range");
+    PHB_REQUIRE(aligned16(ws), PHB_ERR_ALIGN, "workspace must be 16-byte aligned");
+    phb_status st = check_device();
+    if (st != PHB_OK) return st;
+    if (fused) {
+        PHB_CUDA(phb::decode_persistent_probe(ws, d_model, n_q_heads, n_kv_heads, head_dim, d_ff, qkv, x1, act, stream),
+                 "probe launch");
+        return ok();
+    }
+    const DecodeWs w = decode_ws(d_model, n_q_heads, n_kv_heads, head_dim, d_ff, const_cast<void*>(ws));
+    const size_t nqkv = static_cast<size_t>(n_q_heads + 2 * n_kv_heads) * head_dim;
+    PHB_CUDA(cudaMemcpyAsync(qkv, w.qkv, nqkv * sizeof(float), cudaMemcpyDeviceToDevice, stream), "probe copy");
+    PHB_CUDA(cudaMemcpyAsync(x1, w.x1, static_cast<size_t>(d_model) * sizeof(float), cudaMemcpyDeviceToDevice, stream),
+             "probe copy");
+    PHB_CUDA(cudaMemcpyAsync(act, w.act, static_cast<size_t>(d_ff) * sizeof(float), cudaMemcpyDeviceToDevice, stream),
+             "probe copy");
+    return ok();
+}
+
 // ---------------------------------------------------------------- decode attention
 static constexpr int64_t kAttnMaxCtx = int64_t{1} << 26;
 

@@ -316,6 +316,15 @@ struct Rings {
 
 }  // namespace
 
+// Copies the values (low words) of replica 0 of three tagged vectors.
+__global__ void probe_pairs_kernel(const uint2* qkv, int n_qkv, const uint2* x1, int n_dm, const uint2* act, int n_ff,
+                                   float* qkv_out, float* x1_out, float* act_out) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n_qkv) qkv_out[i] = __uint_as_float(qkv[i].x);
+    if (i < n_dm) x1_out[i] = __uint_as_float(x1[i].x);
+    if (i < n_ff) act_out[i] = __uint_as_float(act[i].x);
+}
+
 // Workspace of the persistent step: tagged intermediate vectors and the state words.
 size_t decode_persistent_ws_bytes(int64_t d_model, int n_q, int n_kv, int hd, int64_t d_ff) {
     auto al = [](size_t v) { return (v + 255) & ~size_t{255}; };
@@ -324,6 +333,24 @@ size_t decode_persistent_ws_bytes(int64_t d_model, int n_q, int n_kv, int hd, in
     b += kRep * al(static_cast<size_t>(d_model) * 8) * 3;
     b += kRep * al(static_cast<size_t>(d_ff) * 8);
     return b;
+}
+
+cudaError_t decode_persistent_probe(const void* ws, int64_t d_model, int n_q, int n_kv, int hd, int64_t d_ff,
+                                    float* qkv, float* x1, float* act, cudaStream_t s) {
+    auto al = [](size_t v) { return (v + 255) & ~size_t{255}; };
+    const int qkv_dim = (n_q + 2 * n_kv) * hd;
+    const auto* b = static_cast<const uint8_t*>(ws);
+    const size_t rs_qkv = al(static_cast<size_t>(qkv_dim) * 8), rs_dm = al(static_cast<size_t>(d_model) * 8);
+    size_t off = al(kStateWords * 4);
+    const auto* pq = reinterpret_cast<const uint2*>(b + off);
+    off += kRep * rs_qkv;
+    const auto* px1 = reinterpret_cast<const uint2*>(b + off);
+    off += 3 * kRep * rs_dm;  // x1, then the two layer-output vectors
+    const auto* pact = reinterpret_cast<const uint2*>(b + off);
+    const int n = static_cast<int>(std::max<int64_t>({static_cast<int64_t>(qkv_dim), d_model, d_ff}));
+    probe_pairs_kernel<<<(n + 255) / 256, 256, 0, s>>>(pq, qkv_dim, px1, static_cast<int>(d_model), pact,
+                                                       static_cast<int>(d_ff), qkv, x1, act);
+    return cudaGetLastError();
 }
 
 cudaError_t decode_persistent_run(int qt, const void* const* wl, int n_layers, int64_t d_model, int n_q, int n_kv,

@@ -575,6 +575,9 @@ MoeWs moe_ws_layout(const MoeReq& q, void* base) {
         off = align_up(off + bytes);
         return ptr;
     };
+    // the per-pair outputs and activations lead (a documented part of the ABI)
+    w.yp = reinterpret_cast<float*>(take(pairs * q.d_model * 4));
+    w.h = reinterpret_cast<float*>(take(pairs * q.d_ff * 4));
     w.r.idx = reinterpret_cast<int32_t*>(take(pairs * 4));
     w.r.p = reinterpret_cast<float*>(take(pairs * 4));
     w.r.n_active = reinterpret_cast<int32_t*>(take(16));
@@ -582,8 +585,6 @@ MoeWs moe_ws_layout(const MoeReq& q, void* base) {
     w.r.act_off = reinterpret_cast<int32_t*>(take(slots * 4));
     w.r.act_cnt = reinterpret_cast<int32_t*>(take(slots * 4));
     w.r.pair_list = reinterpret_cast<int32_t*>(take(pairs * 4));
-    w.h = reinterpret_cast<float*>(take(pairs * q.d_ff * 4));
-    w.yp = reinterpret_cast<float*>(take(pairs * q.d_model * 4));
     w.tile_ctr = reinterpret_cast<int*>(take(static_cast<size_t>((q.d_model + kMrRows - 1) / kMrRows) * 4));
     w.bytes = off;
     return w;

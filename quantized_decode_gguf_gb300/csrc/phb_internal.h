@@ -106,6 +106,9 @@ constexpr int kPersistMaxLayers = 64;
 size_t decode_persistent_ws_bytes(int64_t d_model, int n_q, int n_kv, int hd, int64_t d_ff);
 cudaError_t decode_persistent_run(int qt, const void* const* wl, int n_layers, int64_t d_model, int n_q, int n_kv,
                                   int hd, int64_t d_ff, const float* x_in, float* x_out, void* ws, cudaStream_t s);
+// Copies the last layer's qkv, x1 and SwiGLU activation out of a persistent-step workspace.
+cudaError_t decode_persistent_probe(const void* ws, int64_t d_model, int n_q, int n_kv, int hd, int64_t d_ff,
+                                    float* qkv, float* x1, float* act, cudaStream_t s);
 
 // ---------------------------------------------------------------- dequant
 cudaError_t dequant_run(int qt, bool bf16, const void* blocks, void* w, int64_t n, int64_t k, cudaStream_t s);
