@@ -5,9 +5,10 @@ zero quants under a nonzero scale, the int8 value -128, quants in {-1, 0, 1},
 zero scales, Q4_K sub-blocks whose scale term cancels the min term exactly,
 zero 6-bit scales with a nonzero min, and rows that mix such blocks with
 ordinary ones. The contract is the unchanged |err| <= 1e-3 * sum|w x| per
-output element, which demands y == 0 exactly wherever sum|w x| == 0; the
-composed steps use the oracle's propagated bounds, which are zero exactly
-where every term feeding an output is zero.
+output element, which demands y == 0 exactly wherever sum|w x| == 0. The
+composed steps are checked stage by stage from the intermediates the GPU
+used (the bounds of a stage are zero exactly where every term feeding an
+output is zero), and against the end-to-end bounds as well.
 """
 
 import numpy as np
@@ -18,7 +19,9 @@ import oracle
 import quantized_decode_gguf_gb300 as phb
 import synth
 from _edge import edge
-from _helpers import assert_within, check_device_clean, ensure_built, to_dev, to_host
+from _helpers import (assert_stages, assert_within, check_device_clean, ensure_built, ffn_hidden, moe_intermediates,
+                      to_dev, to_host)
+from test_gpu_ffn_moe_decode import check_decode_layer
 
 pytestmark = pytest.mark.gpu
 
@@ -69,11 +72,16 @@ def test_ffn_swiglu_edge_matrices(qtype, d_model, d_ff, batch):
     wu, _ = edge(qtype, seed + 10, d_ff, d_model)
     wd, _ = edge(qtype, seed + 20, d_model, d_ff)
     x = synth.normal_f32(seed, 3, (batch, d_model))
-    y = to_host(phb.ffn_swiglu(qtype, to_dev(wg), to_dev(wu), to_dev(wd), to_dev(x), d_model, d_ff))
-    ref, tol, _ = oracle.swiglu_ffn(oracle.dequant(qtype, wg, d_ff, d_model), oracle.dequant(qtype, wu, d_ff, d_model),
-                                    oracle.dequant(qtype, wd, d_model, d_ff), x)
-    assert (tol == 0).any()
-    assert_within(y, ref, tol, f"edge ffn {qtype} {d_model}->{d_ff} b{batch}")
+    ws = phb.workspace(phb.ffn_workspace_size(qtype, d_model, d_ff, batch))
+    y = to_host(phb.ffn_swiglu(qtype, to_dev(wg), to_dev(wu), to_dev(wd), to_dev(x), d_model, d_ff, ws=ws))
+    mats = (oracle.dequant(qtype, wg, d_ff, d_model), oracle.dequant(qtype, wu, d_ff, d_model),
+            oracle.dequant(qtype, wd, d_model, d_ff))
+    h_dev = ffn_hidden(ws, batch, d_ff)
+    (h, dh), (yr, dy) = oracle.swiglu_stages(*mats, x, h_dev)
+    assert (dh == 0).any() and (dy == 0).any()
+    assert_stages({"h": (h, dh), "y": (yr, dy)}, {"h": h_dev, "y": y}, f"edge ffn {qtype} {d_model}->{d_ff} b{batch}")
+    ref, tol, _ = oracle.swiglu_ffn(*mats, x)
+    assert_within(y, ref, tol, f"edge ffn {qtype} {d_model}->{d_ff} b{batch} end to end")
     check_device_clean()
 
 
@@ -91,17 +99,22 @@ def test_moe_edge_experts(t):
     logits = synth.normal_f32(742, t, (t, e))
     idx = torch.empty((t, k), dtype=torch.int32, device="cuda")
     p = torch.empty((t, k), dtype=torch.float32, device="cuda")
+    ws = phb.moe_workspace(qtype, t, d_model, d_ff, e, k)
     y = to_host(phb.moe_ffn(qtype, to_dev(wg), to_dev(wu), to_dev(wd), to_dev(x), to_dev(logits), d_model, d_ff, e,
-                            k, out_idx=idx, out_p=p))
+                            k, out_idx=idx, out_p=p, ws=ws))
     ridx, _ = oracle.moe_route(logits, k)
     assert np.array_equal(to_host(idx), ridx)
     deq = [tuple(oracle.dequant(qtype, m, r, c) for m, (r, c) in
                  zip(base[i], [(d_ff, d_model), (d_ff, d_model), (d_model, d_ff)])) for i in range(8)]
     used = sorted(set(ridx.ravel().tolist()))
-    ref, tol, _, _ = oracle.moe_ffn({i: deq[i % 8][0] for i in used}, {i: deq[i % 8][1] for i in used},
-                                    {i: deq[i % 8][2] for i in used}, x, logits, k)
+    mg, mu, md = ({i: deq[i % 8][j] for i in used} for j in range(3))
+    h_dev, yp_dev = moe_intermediates(ws, t, k, d_model, d_ff)
+    _, _, hs, yps, comb = oracle.moe_stages(mg, mu, md, x, logits, k, h_dev, yp_dev)
+    assert (yps[1] == 0).any()
+    assert_stages({"h": hs, "y_pair": yps, "y": comb}, {"h": h_dev, "y_pair": yp_dev, "y": y}, f"edge moe T={t}")
+    ref, tol, _, _ = oracle.moe_ffn(mg, mu, md, x, logits, k)
     assert (tol == 0).any()
-    assert_within(y, ref, tol, f"edge moe T={t}")
+    assert_within(y, ref, tol, f"edge moe T={t} end to end")
     check_device_clean()
 
 
@@ -116,8 +129,6 @@ def test_decode_layer_edge_matrices(qtype, fused):
     blobs = [edge(qtype, 760 + i, r, c)[0] for i, (r, c) in enumerate(shapes)]
     table = phb.layer_table([[to_dev(b) for b in blobs]])
     x = synth.normal_f32(760, 99, (D_MODEL,))
-    y = to_host(phb.decode_step(qtype, table, 1, D_MODEL, N_Q, N_KV, HD, D_FF, to_dev(x), fused=fused))
     mats = [oracle.dequant(qtype, b, r, c) for b, (r, c) in zip(blobs, shapes)]
-    ref, bound = oracle.decode_layer(x, np.zeros((1, D_MODEL)), *mats, N_Q, N_KV, HD)
-    assert_within(y[None, :], ref, bound, f"edge decode layer {qtype} fused={fused}")
+    check_decode_layer(qtype, table, mats, x, fused, f"edge decode layer {qtype} fused={fused}")
     check_device_clean()

@@ -1,8 +1,15 @@
 """GPU parity of the SwiGLU FFN, the routed MoE FFN and the dense decode step.
 
-Tolerances are the oracle's propagated bounds (oracle.swiglu_ffn,
-oracle.moe_ffn, oracle.decode_layer) built on the per-GEMV contract
-|err| <= 1e-3 * sum|w x|.
+Each composed step is checked stage by stage: every GEMV inside it against
+the per-GEMV contract |err| <= 1e-3 * sum|w x| for the input the GPU
+actually used (read from the documented workspace prefix, or through
+phb_decode_step_probe), and every elementwise step against its stated
+evaluation error (oracle.swiglu_stages, oracle.moe_stages,
+oracle.decode_layer_stages). The end-to-end bounds that chain the contract
+through two GEMVs (oracle.swiglu_ffn, oracle.moe_ffn) are checked as well;
+they are valid, but at model sizes they grow beyond the outputs, so the
+stage checks carry the parity claim. The decode layer's end-to-end bound
+(four GEMVs deep) is infinite at model sizes and is pinned on the CPU only.
 """
 
 import numpy as np
@@ -12,7 +19,8 @@ import torch
 import oracle
 import quantized_decode_gguf_gb300 as phb
 import synth
-from _helpers import assert_within, check_device_clean, ensure_built, to_dev, to_host
+from _helpers import (assert_stages, assert_within, check_device_clean, ensure_built, ffn_hidden, moe_intermediates,
+                      to_dev, to_host)
 
 pytestmark = pytest.mark.gpu
 
@@ -43,10 +51,15 @@ def test_ffn_swiglu_within_bound(qtype, d_model, d_ff, batch):
     wu = synth.blocks(qtype, seed, 1, d_ff, d_model)
     wd = synth.blocks(qtype, seed, 2, d_model, d_ff)
     x = synth.normal_f32(seed, 3, (batch, d_model))
-    y = to_host(phb.ffn_swiglu(qtype, to_dev(wg), to_dev(wu), to_dev(wd), to_dev(x), d_model, d_ff))
-    ref, tol, _ = oracle.swiglu_ffn(oracle.dequant(qtype, wg, d_ff, d_model), oracle.dequant(qtype, wu, d_ff, d_model),
-                                    oracle.dequant(qtype, wd, d_model, d_ff), x)
-    assert_within(y, ref, tol, f"ffn {qtype} {d_model}->{d_ff} b{batch}")
+    ws = phb.workspace(phb.ffn_workspace_size(qtype, d_model, d_ff, batch))
+    y = to_host(phb.ffn_swiglu(qtype, to_dev(wg), to_dev(wu), to_dev(wd), to_dev(x), d_model, d_ff, ws=ws))
+    mats = (oracle.dequant(qtype, wg, d_ff, d_model), oracle.dequant(qtype, wu, d_ff, d_model),
+            oracle.dequant(qtype, wd, d_model, d_ff))
+    h_dev = ffn_hidden(ws, batch, d_ff)
+    (h, dh), (yr, dy) = oracle.swiglu_stages(*mats, x, h_dev)
+    assert_stages({"h": (h, dh), "y": (yr, dy)}, {"h": h_dev, "y": y}, f"ffn {qtype} {d_model}->{d_ff} b{batch}")
+    ref, tol, _ = oracle.swiglu_ffn(*mats, x)
+    assert_within(y, ref, tol, f"ffn {qtype} {d_model}->{d_ff} b{batch} end to end")
     check_device_clean()
 
 
@@ -75,12 +88,12 @@ def _deq_experts(qtype, blobs, rows, cols):
     return np.stack([oracle.dequant(qtype, b, rows, cols) for b in blobs])
 
 
-def _run_moe(qtype, wg, wu, wd, x, logits, d_model, d_ff, e, k):
+def _run_moe(qtype, wg, wu, wd, x, logits, d_model, d_ff, e, k, ws=None):
     t = x.shape[0]
     idx = torch.empty((t, k), dtype=torch.int32, device="cuda")
     p = torch.empty((t, k), dtype=torch.float32, device="cuda")
     y = phb.moe_ffn(qtype, to_dev(wg), to_dev(wu), to_dev(wd), to_dev(x), to_dev(logits), d_model, d_ff, e, k,
-                    out_idx=idx, out_p=p)
+                    out_idx=idx, out_p=p, ws=ws)
     return to_host(y), to_host(idx), to_host(p)
 
 
@@ -101,17 +114,22 @@ def test_moe_ffn_within_bound(qtype, t, e, k, d_model, d_ff):
     wg, wu, wd = _experts(qtype, seed, e, d_model, d_ff)
     x = synth.normal_f32(seed, 10_000, (t, d_model))
     logits = synth.normal_f32(seed, 10_001, (t, e))
-    y, idx, p = _run_moe(qtype, wg, wu, wd, x, logits, d_model, d_ff, e, k)
+    ws = phb.moe_workspace(qtype, t, d_model, d_ff, e, k)
+    y, idx, p = _run_moe(qtype, wg, wu, wd, x, logits, d_model, d_ff, e, k, ws=ws)
     ridx, rp = oracle.moe_route(logits, k)
     assert np.array_equal(idx, ridx), "routing differs from the oracle"
     assert np.allclose(p, rp, rtol=1e-6, atol=0)
-    # the oracle's MoE block and bound; only the routed experts are dequantised
+    # the oracle's MoE block and bounds; only the routed experts are dequantised
     used = sorted(set(ridx.ravel().tolist()))
     dg = {i: oracle.dequant(qtype, wg[i], d_ff, d_model) for i in used}
     du = {i: oracle.dequant(qtype, wu[i], d_ff, d_model) for i in used}
     dd = {i: oracle.dequant(qtype, wd[i], d_model, d_ff) for i in used}
+    h_dev, yp_dev = moe_intermediates(ws, t, k, d_model, d_ff)
+    _, _, hs, yps, comb = oracle.moe_stages(dg, du, dd, x, logits, k, h_dev, yp_dev)
+    assert_stages({"h": hs, "y_pair": yps, "y": comb}, {"h": h_dev, "y_pair": yp_dev, "y": y},
+                  f"moe {qtype} T={t} E={e} k={k}")
     ref, tol, _, _ = oracle.moe_ffn(dg, du, dd, x, logits, k)
-    assert_within(y, ref, tol, f"moe {qtype} T={t} E={e} k={k}")
+    assert_within(y, ref, tol, f"moe {qtype} T={t} E={e} k={k} end to end")
     check_device_clean()
 
 
@@ -190,16 +208,27 @@ def _deq_layer(qtype, blobs):
     return [oracle.dequant(qtype, b, r, c) for b, (r, c) in zip(blobs, shapes)]
 
 
+def check_decode_layer(qtype, table, mats, x, fused, what):
+    """One decode layer through the library, checked stage by stage from the
+    intermediates the GPU used (phb_decode_step_probe); returns the output."""
+    ws = phb.decode_workspace(qtype, D_MODEL, N_Q, N_KV, HD, D_FF)
+    y = to_host(phb.decode_step(qtype, table, 1, D_MODEL, N_Q, N_KV, HD, D_FF, to_dev(x), ws=ws, fused=fused))
+    qkv, x1, act = (to_host(v) for v in phb.decode_step_probe(ws, D_MODEL, N_Q, N_KV, HD, D_FF, fused=fused))
+    st = oracle.decode_layer_stages(x, qkv, x1, act, *mats, N_Q, N_KV, HD)
+    assert_stages(st, {"qkv": qkv, "x1": x1, "act": act, "out": y}, what)
+    # (the end-to-end bound of oracle.decode_layer is infinite at these sizes:
+    # the allowance chained through the QKV and O GEMVs exceeds the second
+    # RMSNorm's input itself, so it says nothing and is not checked here)
+    return y
+
+
 @pytest.mark.parametrize("fused", [True, False])
 @pytest.mark.parametrize("qtype", ["q8_0", "q4_k"])
 def test_decode_single_layer_within_bound(qtype, fused):
     blobs = _layer_blobs(qtype, 600, 0)
-    dev = [to_dev(b) for b in blobs]
-    table = phb.layer_table([dev])
+    table = phb.layer_table([[to_dev(b) for b in blobs]])
     x = synth.normal_f32(600, 999, (D_MODEL,))
-    y = to_host(phb.decode_step(qtype, table, 1, D_MODEL, N_Q, N_KV, HD, D_FF, to_dev(x), fused=fused))
-    ref, bound = oracle.decode_layer(x, np.zeros((1, D_MODEL)), *_deq_layer(qtype, blobs), N_Q, N_KV, HD)
-    assert_within(y[None, :], ref, bound, f"decode layer {qtype} fused={fused}")
+    check_decode_layer(qtype, table, _deq_layer(qtype, blobs), x, fused, f"decode layer {qtype} fused={fused}")
     check_device_clean()
 
 
@@ -248,9 +277,9 @@ def test_fused_decode_in_a_cuda_graph_replays():
 
 def test_decode_24_layers_layerwise_and_composed():
     """The 24-layer step equals 24 chained single-layer steps bit for bit, and
-    every layer is within its bound of the oracle layer applied to the same
-    (GPU-produced) input. A worst-case bound propagated through 24 random
-    layers grows by orders of magnitude per layer, so each layer is checked
+    every GEMV of every layer is within its contract of the oracle applied to
+    the GPU's own input to it. A worst-case bound propagated through the
+    chain grows by orders of magnitude per GEMV, so each stage is checked
     from its own input instead (errors do not compound)."""
     qtype, n_layers = "q8_0", 24
     seed = synth.workload_seed(1)
@@ -263,10 +292,8 @@ def test_decode_24_layers_layerwise_and_composed():
     ref_chain = x.astype(np.float64)[None, :]
     for layer in range(n_layers):
         one = phb.layer_table([dev_layers[layer]])
-        nxt = to_host(phb.decode_step(qtype, one, 1, D_MODEL, N_Q, N_KV, HD, D_FF, to_dev(cur)))
         mats = _deq_layer(qtype, blobs[layer])
-        ref, bound = oracle.decode_layer(cur, np.zeros((1, D_MODEL)), *mats, N_Q, N_KV, HD)
-        assert_within(nxt[None, :], ref, bound, f"layer {layer}")
+        nxt = check_decode_layer(qtype, one, mats, cur, True, f"layer {layer}")
         ref_chain, _ = oracle.decode_layer(ref_chain, np.zeros((1, D_MODEL)), *mats, N_Q, N_KV, HD)
         cur = nxt
     assert np.array_equal(y, cur), "24-layer call differs from 24 chained single-layer calls"
