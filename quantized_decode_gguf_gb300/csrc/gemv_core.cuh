@@ -66,13 +66,6 @@ __device__ __forceinline__ void q8_0_mult(float d, float& a, float& c) {
     c = d * -0x1p-78f;
 }
 
-// Multipliers of one Q4_K sub-block: a = d * sc * 2^64, c = -dmin * m * 2^-85
-// (d*sc and dmin*m have at most 17 significant bits: exact).
-__device__ __forceinline__ void q4_k_mult(float d, float dmin, uint32_t sc, uint32_t m, float& a, float& c) {
-    a = (d * 0x1p64f) * static_cast<float>(sc);
-    c = (dmin * -0x1p-85f) * static_cast<float>(m);
-}
-
 // Rows b >= batch of the staged activations are zero, so the loops below run
 // over all MAXB rows without guards.
 // Activation layout in shared memory: a pad of 4 floats after every 128, so
@@ -180,16 +173,26 @@ __device__ __forceinline__ void q4_k_scale_min(const uint32_t (&sw)[3], int j, u
     q4_k_scale_min_half(sw, j >> 2, j & 3, sc, m);
 }
 
-// Multipliers of the four sub-blocks 4h..4h+3 of a Q4_K block header.
+// Multipliers of the four sub-blocks 4h..4h+3 of a Q4_K block header, with
+// the scale and min bytes extracted word-wide: for h = 0 the low 6 bits of
+// scale bytes 0-3 (scales) and 4-7 (mins); for h = 1 the low (scales) or high
+// (mins) nibbles of bytes 8-11 with bits 6-7 of bytes 0-3 (scales) or 4-7
+// (mins) on top. A 6-bit value v in byte jj of a word becomes the float v
+// exactly as (2^23 + v) - 2^23.
 __device__ __forceinline__ void q4_k_half_mults(const uint4& hdr, int h, float (&a)[4], float (&c)[4]) {
     const float d = fp16_bits_to_float(hdr.x);
     const float dmin = fp16_bits_to_float(hdr.x >> 16);
-    const uint32_t sw[3] = {hdr.y, hdr.z, hdr.w};
+    const uint32_t sc0 = hdr.y & 0x3F3F3F3Fu, m0 = hdr.z & 0x3F3F3F3Fu;
+    const uint32_t sc1 = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
+    const uint32_t m1 = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
+    const uint32_t scb = h ? sc1 : sc0, mb = h ? m1 : m0;
+    const float ds = d * 0x1p64f, dm = dmin * -0x1p-85f;
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
-        uint32_t sc, m;
-        q4_k_scale_min_half(sw, h, jj, sc, m);
-        q4_k_mult(d, dmin, sc, m, a[jj], c[jj]);
+        const float scf = __uint_as_float(__byte_perm(scb, 0x4B000000u, 0x7440u | jj)) - 8388608.0f;
+        const float mf = __uint_as_float(__byte_perm(mb, 0x4B000000u, 0x7440u | jj)) - 8388608.0f;
+        a[jj] = ds * scf;  // d * sc * 2^64, exact
+        c[jj] = dm * mf;   // -dmin * m * 2^-85, exact
     }
 }
 
@@ -197,7 +200,9 @@ __device__ __forceinline__ void q4_k_half_mults(const uint4& hdr, int h, float (
 //   blk:  the 144-byte block (16-byte aligned)
 //   xs, xfac: as for Q8_0
 // Quant byte i of 64-weight chunk cc holds weight i of sub-block 2cc in its
-// low nibble and weight i of sub-block 2cc + 1 in its high nibble.
+// low nibble and weight i of sub-block 2cc + 1 in its high nibble. The high
+// nibbles are masked in place (the byte is then 16 q) and the factor 1/16
+// goes into that sub-block's multiplier, which stays exact.
 template <int MAXB>
 __device__ __forceinline__ void dot_q4_k_half(const uint8_t* blk, int h, const float* xs, int xstride,
                                               const float* xfac, float (&acc)[MAXB]) {
@@ -218,12 +223,12 @@ __device__ __forceinline__ void dot_q4_k_half(const uint8_t* blk, int h, const f
     for (int b = 0; b < MAXB; ++b) s2[b] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc) {
-        const float al = a[2 * cc], cl = c[2 * cc], ah = a[2 * cc + 1], ch = c[2 * cc + 1];
+        const float al = a[2 * cc], cl = c[2 * cc], ah = a[2 * cc + 1] * 0.0625f, ch = c[2 * cc + 1];
 #pragma unroll
         for (int wi = 0; wi < 8; ++wi) {
             const uint32_t w = qw[8 * cc + wi];
             const uint32_t lo = w & 0x0F0F0F0Fu;
-            const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;
+            const uint32_t hi = w & 0xF0F0F0F0u;
             const float2 l01 = wpair(al, byte_subnormal<0>(lo), byte_subnormal<1>(lo), cl);
             const float2 l23 = wpair(al, byte_subnormal<2>(lo), byte_subnormal<3>(lo), cl);
             const float2 h01 = wpair(ah, byte_subnormal<0>(hi), byte_subnormal<1>(hi), ch);
@@ -261,12 +266,12 @@ __device__ __forceinline__ float dot_q4_k_half_xr(const uint8_t* blk, int h, con
     float2 s2 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc) {
-        const float al = a[2 * cc], cl = c[2 * cc], ah = a[2 * cc + 1], ch = c[2 * cc + 1];
+        const float al = a[2 * cc], cl = c[2 * cc], ah = a[2 * cc + 1] * 0.0625f, ch = c[2 * cc + 1];
 #pragma unroll
         for (int wi = 0; wi < 8; ++wi) {
             const uint32_t w = qw[8 * cc + wi];
             const uint32_t lo = w & 0x0F0F0F0Fu;
-            const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;
+            const uint32_t hi = w & 0xF0F0F0F0u;
             const int kl = 64 * cc + 4 * wi, kh = kl + 32;
             s2 = __ffma2_rn(wpair(al, byte_subnormal<0>(lo), byte_subnormal<1>(lo), cl), make_float2(xr[kl], xr[kl + 1]), s2);
             s2 = __ffma2_rn(wpair(al, byte_subnormal<2>(lo), byte_subnormal<3>(lo), cl), make_float2(xr[kl + 2], xr[kl + 3]), s2);
