@@ -164,6 +164,7 @@ cudaError_t gemv_run(const GemvReq& q, cudaStream_t s) {
         }
     }
     if (q.xmode != kXPlain) return cudaErrorInvalidValue;
+    if (gemv_xr_fits(q)) return gemv_xr_run(q, s);
     if (use_rows_kernel(q)) {
         int ks = 1;
         cudaError_t e = gemv_rows_run(q, s, &ks);

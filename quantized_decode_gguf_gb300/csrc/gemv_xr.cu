@@ -1,0 +1,247 @@
+// Batch-1 streaming GEMV with register-resident activations.
+//
+// The streaming kernel of gemv_kernel.cuh reads one activation from shared
+// memory per weight and stages the activation vector with a CTA-wide scale
+// reduction. At batch 1 both show: the dot runs at about half the rate of a
+// dot whose activations sit in registers, and staging costs two barriers.
+// Here every stage holds whole row segments (a gate/up pair counting as
+// two), so consumer thread t works on segment t / (2 useg) and on the same
+// half-unit position pos = t % (2 useg) of every stage. The CTA reads x once
+// (coalesced, each element once) into shared memory; after one barrier every
+// thread copies its 128 activations x[128 pos .. 128 pos + 127] into
+// registers, scaled by a power of two 2^s chosen from their own largest
+// magnitude, and undoes the scale per half-unit sum (xfac = 2^(85 - s)) before
+// anything is added across threads. No CTA-wide reduction stands between the
+// previous kernel's end and the first dot. (Every thread reading its slice
+// from global memory itself funnels the whole grid onto the few L2 lines
+// that hold x: measured several times slower.)
+//
+// Half-unit sums go to shared memory; after the last stage one thread per row
+// adds them in position order (deterministic) and runs the epilogue: store,
+// or silu(gate) * up for the fused pair. A producer warp streams the CTA's
+// row slice through a ring of stages with bulk copies (before the
+// programmatic-dependent-launch wait: weights never depend on the previous
+// kernel) and optionally prefetches later kernels' weights into L2.
+#include "gemv_plan.cuh"
+#include "phb_internal.h"
+
+namespace phb {
+
+cudaError_t read_dev_err_gemv_xr(int* code) {
+    int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_dev_err, sizeof(int));
+    if (e != cudaSuccess) return e;
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_dev_err, &zero, sizeof(int));
+    *code = v;
+    return e;
+}
+
+#ifdef PHB_TRACE
+// Debug builds only: copy out this unit's per-CTA timestamps.
+extern "C" int phb_trace_read_gemv_xr(void* dst, size_t bytes) {
+    if (bytes > sizeof(g_trace)) bytes = sizeof(g_trace);
+    return static_cast<int>(cudaMemcpyFromSymbol(dst, g_trace, bytes));
+}
+#endif
+
+namespace {
+
+constexpr int kXrNS = 4;  // ring stages
+
+struct XrParams {
+    const uint8_t* w[2];
+    int64_t row_bytes;
+    int64_t n;
+    int useg;          // units per row (K / 256)
+    int rows_per_cta;
+    int segs;          // segments per stage
+    const float* x;
+    float* y;
+    const uint8_t* pf[2];
+    int64_t pf_bytes[2];
+    uint32_t xs_off, part_off, bar_off;
+    int trace_id;      // launch id for debug tracing builds (-1: none)
+};
+
+template <int QT, int NMAT, int CW>
+__global__ void __launch_bounds__(32 * CW + 32, CW <= 6 ? 2 : 1) gemv_xr_kernel(const __grid_constant__ XrParams p) {
+    using C = KCfg<QT, CW, kXrNS>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    float* xs = reinterpret_cast<float*>(smem + p.xs_off);  // x in the padded layout (xpad_idx)
+    float* part = reinterpret_cast<float*>(smem + p.part_off);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
+    uint64_t* empty = full + kXrNS;
+
+    const int tid = threadIdx.x, lane = tid & 31;
+    if (tid == 0) PHB_TRACE_EV(p.trace_id, 0);
+    const int64_t row0 = static_cast<int64_t>(blockIdx.x) * p.rows_per_cta;
+    Tile t;
+    t.rows_here = static_cast<int>(min(static_cast<int64_t>(p.rows_per_cta), p.n - row0));
+    t.useg = p.useg;
+    t.row_bytes = p.row_bytes;
+    t.contiguous = true;
+    t.w[0] = p.w[0] + row0 * p.row_bytes;
+    t.w[1] = p.w[NMAT - 1] + row0 * p.row_bytes;
+    pdl_launch_dependents();
+    if (t.rows_here <= 0) return;
+
+    if (tid == 0) {
+        for (int s = 0; s < kXrNS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], CW);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (tid >= C::consumers) {
+        if (tid == C::consumers) {
+            int s = 0;
+            produce_tile<QT, CW, kXrNS>(t, NMAT, smem, full, empty, s, policy_evict_first(), p.segs * t.useg);
+        } else if (tid == C::consumers + 1) {
+            prefetch_share(p.pf[0], p.pf_bytes[0]);
+            prefetch_share(p.pf[1], p.pf_bytes[1]);
+        }
+        return;
+    }
+
+    const int seg_half = 2 * t.useg;
+    const int j = tid / seg_half, pos = tid - j * seg_half;
+    const bool active = j < p.segs;
+    pdl_wait();  // x may come from the previous kernel
+    if (tid == 0) PHB_TRACE_EV(p.trace_id, 1);
+    {
+        const int n4 = t.useg * (kUnitWeights / 4);
+        const float4* xg = reinterpret_cast<const float4*>(p.x);
+        for (int i = tid; i < n4; i += C::consumers)
+            *reinterpret_cast<float4*>(xs + xpad_idx(4 * i)) = __ldcg(xg + i);  // written by the previous kernel
+    }
+    consumer_sync<C::consumers>();
+    float xr[128];
+    float xf = 1.f;
+    if (active) {
+        const float* xp = xs + pos * (kXPadEvery + kXPad);
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const float4 v = *reinterpret_cast<const float4*>(xp + 4 * i);
+            xr[4 * i] = v.x;
+            xr[4 * i + 1] = v.y;
+            xr[4 * i + 2] = v.z;
+            xr[4 * i + 3] = v.w;
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+        }
+        const int se = pick_scale_exp(amax);
+        const int e1 = min(se, 127);
+        const float f1 = __int_as_float((e1 + 127) << 23);
+#pragma unroll
+        for (int i = 0; i < 128; ++i) xr[i] *= f1;
+        if (se > 127) {  // largest magnitude below 2^-3: the rest of the power of two
+            const float f2 = __int_as_float((se - e1 + 127) << 23);
+#pragma unroll
+            for (int i = 0; i < 128; ++i) xr[i] *= f2;
+        }
+        xf = __int_as_float((kWShift - se + 127) << 23);
+    }
+    if (tid == 0) PHB_TRACE_EV(p.trace_id, 2);
+
+    const int nseg = NMAT * t.rows_here;
+    int s = 0;
+    bool ok = true;
+    for (int seg0 = 0; seg0 < nseg; seg0 += p.segs, ++s) {
+        const int slot = s % kXrNS;
+        if (!mbar_wait_warp(&full[slot], (s / kXrNS) & 1, &g_dev_err)) {
+            mbar_wait(&full[slot], (s / kXrNS) & 1, &g_dev_err);  // second bounded wait for the copy in flight
+            ok = false;
+            break;
+        }
+        const int seg = seg0 + j;
+        if (active && seg < nseg) {
+            const uint8_t* ub = smem + slot * C::stage_bytes + (j * t.useg + (pos >> 1)) * C::ub;
+            float acc;
+            if constexpr (QT == 0)
+                acc = dot_q8_0_half_xr(ub + 136 * (pos & 1), xr, xf);
+            else
+                acc = dot_q4_k_half_xr(ub, pos & 1, xr, xf);
+            part[seg * seg_half + pos] = acc;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+    }
+    if (tid == 0) PHB_TRACE_EV(p.trace_id, 3);
+    consumer_sync<C::consumers>();
+    if (!ok) return;
+    for (int r = tid; r < t.rows_here; r += C::consumers) {
+        float a[NMAT];
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m) {
+            const float* q = part + static_cast<size_t>(r * NMAT + m) * seg_half;
+            float v = 0.f;
+            for (int h = 0; h < seg_half; ++h) v += q[h];
+            a[m] = v;
+        }
+        p.y[row0 + r] = NMAT == 2 ? silu_mul(a[0], a[NMAT - 1]) : a[0];
+    }
+    if (tid == 0) PHB_TRACE_EV(p.trace_id, 4);
+}
+
+template <int QT, int NMAT, int CW>
+cudaError_t launch_xr(const XrParams& p, dim3 grid, size_t smem, cudaStream_t s, bool pdl) {
+    constexpr auto kern = gemv_xr_kernel<QT, NMAT, CW>;
+    cudaError_t e = ensure_smem_attr<kern>();
+    if (e != cudaSuccess) return e;
+    return launch_kernel(kern, grid, dim3(32 * CW + 32), smem, s, pdl, p);
+}
+
+// Consumer warps per CTA and CTAs per SM of the register-resident kernel.
+constexpr int kXrCW = 5;
+constexpr int kXrCtasPerSm = 2;
+
+}  // namespace
+
+bool gemv_xr_fits(const GemvReq& q) {
+    if (q.batch != 1 || q.xmode != kXPlain || q.k % kUnitWeights != 0) return false;
+    if (!((q.nmat == 1 && q.epi == kEpiStore) || (q.nmat == 2 && q.epi == kEpiSwiGLU))) return false;
+    const int seg_half = static_cast<int>(2 * (q.k / kUnitWeights));
+    return q.nmat * seg_half <= 32 * kXrCW;  // a stage holds at least one row (pair) segment
+}
+
+cudaError_t gemv_xr_run(const GemvReq& q, cudaStream_t s) {
+    if (!gemv_xr_fits(q)) return cudaErrorInvalidValue;
+    const int useg = static_cast<int>(q.k / kUnitWeights);
+    const int seg_half = 2 * useg;
+    const int consumers = 32 * kXrCW;
+    XrParams p{};
+    p.w[0] = static_cast<const uint8_t*>(q.w0);
+    p.w[1] = static_cast<const uint8_t*>(q.nmat == 2 ? q.w1 : q.w0);
+    p.row_bytes = static_cast<int64_t>(useg) * (q.qt == 0 ? Fmt<0>::unit_bytes : Fmt<1>::unit_bytes);
+    p.n = q.n;
+    p.useg = useg;
+    p.segs = (consumers / (q.nmat * seg_half)) * q.nmat;
+    const int64_t ctas = std::min<int64_t>(q.n, static_cast<int64_t>(device_sm_count()) * kXrCtasPerSm);
+    p.rows_per_cta = static_cast<int>(cdiv(q.n, ctas));
+    p.x = q.x;
+    p.y = q.y;
+    p.trace_id = q.trace_id;
+    for (int i = 0; i < 2; ++i) {
+        p.pf[i] = static_cast<const uint8_t*>(q.pf[i]);
+        p.pf_bytes[i] = q.pf_bytes[i];
+    }
+    const size_t stage = static_cast<size_t>(16 * kXrCW) * (q.qt == 0 ? Fmt<0>::unit_bytes : Fmt<1>::unit_bytes);
+    size_t off = kXrNS * stage;
+    p.xs_off = static_cast<uint32_t>(off);
+    off += static_cast<size_t>(xpad_len(static_cast<int>(q.k))) * sizeof(float);
+    p.part_off = static_cast<uint32_t>(off);
+    off += static_cast<size_t>(q.nmat) * p.rows_per_cta * seg_half * sizeof(float);
+    off = (off + 15) & ~size_t{15};
+    p.bar_off = static_cast<uint32_t>(off);
+    off += 2 * kXrNS * sizeof(uint64_t);
+    if (off > kSmemOptin) return cudaErrorInvalidConfiguration;
+    const dim3 grid(static_cast<unsigned>(cdiv(q.n, p.rows_per_cta)));
+    if (q.qt == 0)
+        return q.nmat == 2 ? launch_xr<0, 2, kXrCW>(p, grid, off, s, q.pdl) : launch_xr<0, 1, kXrCW>(p, grid, off, s, q.pdl);
+    return q.nmat == 2 ? launch_xr<1, 2, kXrCW>(p, grid, off, s, q.pdl) : launch_xr<1, 1, kXrCW>(p, grid, off, s, q.pdl);
+}
+
+}  // namespace phb

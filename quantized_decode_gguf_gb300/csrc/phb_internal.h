@@ -92,6 +92,10 @@ size_t gemv_ws_floats(const GemvReq& q);
 // batch 1..8; K % 256 == 0 uses the streaming kernel, other Q8_0 K the
 // generic one.
 cudaError_t gemv_run(const GemvReq& q, cudaStream_t s);
+// Batch-1 plain GEMV or fused gate/up with activations held in registers
+// (gemv_xr.cu): whether a request fits it, and the launch.
+bool gemv_xr_fits(const GemvReq& q);
+cudaError_t gemv_xr_run(const GemvReq& q, cudaStream_t s);
 // h[b][j] = silu(g[b][j]) * u[b][j] (unfused SwiGLU for shapes the fused
 // kernel does not take).
 cudaError_t swiglu_run(const float* g, const float* u, float* h, int64_t count, cudaStream_t s);
@@ -153,6 +157,7 @@ cudaError_t read_dev_err_prefill(int* code);
 cudaError_t read_dev_err_decode_persistent(int* code);
 cudaError_t read_dev_err_gemv_rows(int* code);
 cudaError_t read_dev_err_attention(int* code);
+cudaError_t read_dev_err_gemv_xr(int* code);
 
 // Row-resident batched GEMV (gemv_rows.cu): plain store, batch 2..8,
 // K % 256 == 0. ksplit_out receives the K splits (> 1: partials in q.ws
