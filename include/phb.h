@@ -61,7 +61,8 @@ typedef enum phb_status {
     PHB_ERR_WORKSPACE = 4,          /* ws too small (or NULL while ws is needed) */
     PHB_ERR_CUDA = 5,               /* a CUDA runtime call failed; see phb_last_error() */
     PHB_ERR_UNSUPPORTED_DEVICE = 6, /* current device is not compute capability 10.3 */
-    PHB_ERR_DEVICE_TIMEOUT = 7      /* a kernel's bounded wait ran out (phb_device_error) */
+    PHB_ERR_DEVICE_TIMEOUT = 7,     /* a kernel's bounded wait ran out (phb_device_error) */
+    PHB_ERR_DEVICE_INPUT = 8        /* a kernel found a device-side input out of range (phb_device_error) */
 } phb_status;
 
 /* GGUF tensor type ids of the two formats. */
@@ -82,8 +83,10 @@ const char* phb_last_error(void);
 size_t phb_row_bytes(int qtype, int64_t k);
 
 /* Reads and clears the device-side error word that kernels set when a
- * bounded wait runs out. Synchronises the current device. *code receives 0
- * when no kernel reported an error. */
+ * bounded wait runs out (bit 0, PHB_ERR_DEVICE_TIMEOUT) or when a device-side
+ * input is out of range (bit 1, PHB_ERR_DEVICE_INPUT: a tiered expert's
+ * location outside both copies). Synchronises the current device. *code
+ * receives 0 when no kernel reported an error. */
 phb_status phb_device_error(int* code);
 
 /* ---------------------------------------------------------------------------
@@ -166,6 +169,38 @@ phb_status phb_moe_ffn(int qtype, const void* Wgate, const void* Wup, const void
                        int64_t n_tokens, int64_t d_model, int64_t d_ff, int n_experts, int top_k,
                        int32_t* out_idx, float* out_p,
                        void* ws, size_t ws_bytes, phb_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Routed MoE FFN with tiered experts (Phobos README, intro: MoE decode keeps
+ * an expert cache sized by free device memory, and experts that do not fit
+ * stay outside it; the author's feed: decode keeps most of its speed with
+ * part of the memory taken). Same result as phb_moe_ffn, bit for bit, with
+ * each expert's three matrices read from one of two copies:
+ *   expert_loc[e] >= 0: slot expert_loc[e] of the device cache
+ *       Wgate, Wup [n_dev_slots][d_ff][d_model], Wdown [n_dev_slots][d_model][d_ff];
+ *   expert_loc[e] < 0:  entry -1 - expert_loc[e] of the host copy
+ *       Wgate_host, Wup_host [n_host][d_ff][d_model], Wdown_host [n_host][d_model][d_ff].
+ * expert_loc: DEVICE array [n_experts] int32. The host copy must be memory
+ * the GPU can read: pinned (cudaMallocHost / cudaHostAlloc) or registered
+ * (cudaHostRegister) host memory, or any host memory on a device that reads
+ * pageable memory (a Grace system over NVLink-C2C); otherwise
+ * PHB_ERR_INVALID_ARG. Nothing runs on the CPU: after routing, a fetch
+ * kernel copies each active expert that lives only in the host copy into a
+ * staging slot of the workspace (the GPU reads the host memory directly),
+ * and the expert passes read each active expert from the cache or the
+ * staging slot. A location outside both copies reads nothing and is
+ * reported by phb_device_error (PHB_ERR_DEVICE_INPUT). Other arguments,
+ * limits, the workspace rules (zero it before the first call) and the
+ * documented workspace prefix are those of phb_moe_ffn; the workspace adds
+ * min(n_experts, n_tokens * top_k) staging slots of one expert each.
+ * ------------------------------------------------------------------------- */
+size_t phb_moe_ffn_tiered_workspace_size(int qtype, int64_t n_tokens, int64_t d_model, int64_t d_ff,
+                                         int n_experts, int top_k);
+phb_status phb_moe_ffn_tiered(int qtype, const void* Wgate, const void* Wup, const void* Wdown, int n_dev_slots,
+                              const void* Wgate_host, const void* Wup_host, const void* Wdown_host, int n_host,
+                              const int32_t* expert_loc, const float* X, const float* router_logits, float* Y,
+                              int64_t n_tokens, int64_t d_model, int64_t d_ff, int n_experts, int top_k,
+                              int32_t* out_idx, float* out_p, void* ws, size_t ws_bytes, phb_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Prompt-processing GEMM (Phobos README: `phobos-bench` pp<N>; the

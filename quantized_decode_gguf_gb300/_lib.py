@@ -37,6 +37,10 @@ SIGNATURES = {
     "phb_moe_ffn_workspace_size": (_c_sz, [_c_int, _c_i64, _c_i64, _c_i64, _c_int, _c_int]),
     "phb_moe_ffn": (_c_int, [_c_int, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64, _c_int,
                              _c_int, _c_vp, _c_vp, _c_vp, _c_sz, _c_vp]),
+    "phb_moe_ffn_tiered_workspace_size": (_c_sz, [_c_int, _c_i64, _c_i64, _c_i64, _c_int, _c_int]),
+    "phb_moe_ffn_tiered": (_c_int, [_c_int, _c_vp, _c_vp, _c_vp, _c_int, _c_vp, _c_vp, _c_vp, _c_int, _c_vp, _c_vp,
+                                    _c_vp, _c_vp, _c_i64, _c_i64, _c_i64, _c_int, _c_int, _c_vp, _c_vp, _c_vp, _c_sz,
+                                    _c_vp]),
     "phb_gemm_q_prefill_workspace_size": (_c_sz, [_c_int, _c_i64, _c_i64, _c_i64]),
     "phb_gemm_q_prefill": (_c_int, [_c_int, _c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64, _c_vp, _c_sz, _c_vp]),
     "phb_ffn_swiglu_noalloc_max_scratch": (_c_sz, []),

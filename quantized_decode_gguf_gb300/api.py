@@ -52,6 +52,17 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
     return t.data_ptr()
 
 
+def _host_ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    """Address of a pinned, contiguous CPU tensor (memory the GPU can read)."""
+    if t is None:
+        return None
+    if t.is_cuda or not t.is_pinned():
+        raise ValueError("host tensor must be a pinned CPU tensor")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return t.data_ptr()
+
+
 def _stream() -> int:
     return torch.cuda.current_stream().cuda_stream
 
@@ -66,10 +77,11 @@ def workspace(nbytes: int, device=None) -> torch.Tensor:
 
 
 def device_error() -> int:
-    """Read and clear the kernels' device error word (synchronises)."""
+    """Read and clear the kernels' device error word (synchronises): 0, or bit 0
+    (a bounded wait ran out) and bit 1 (a device-side input out of range)."""
     code = ctypes.c_int(0)
     st = _lib.load().phb_device_error(ctypes.byref(code))
-    if st not in (0, 7):
+    if st not in (0, 7, 8):
         _check(st)
     return code.value
 
@@ -158,6 +170,34 @@ def moe_ffn(qtype, w_gate, w_up, w_down, x: torch.Tensor, logits: torch.Tensor, 
 
 
 # ---------------------------------------------------------------- prefill GEMM
+
+def moe_tiered_workspace(qtype, n_tokens: int, d_model: int, d_ff: int, n_experts: int, top_k: int, device=None):
+    """Zeroed workspace for :func:`moe_ffn_tiered` (it carries counters that start at zero)."""
+    n = int(_lib.load().phb_moe_ffn_tiered_workspace_size(qtype_id(qtype), n_tokens, d_model, d_ff, n_experts, top_k))
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+
+
+def moe_ffn_tiered(qtype, w_gate, w_up, w_down, w_gate_host, w_up_host, w_down_host, expert_loc: torch.Tensor,
+                   x: torch.Tensor, logits: torch.Tensor, d_model: int, d_ff: int, n_experts: int, top_k: int,
+                   out: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
+                   out_idx: Optional[torch.Tensor] = None, out_p: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """phb_moe_ffn_tiered: ``w_*`` the device expert cache [slots, ...] (or None), ``w_*_host`` the
+    host copy [n_host, ...] in pinned CPU memory (or None), ``expert_loc`` int32 [n_experts] on the
+    device (slot >= 0, or -1 - host index)."""
+    qt = qtype_id(qtype)
+    t = x.shape[0] if x.dim() == 2 else 1
+    if out is None:
+        out = torch.empty((t, d_model), dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = moe_tiered_workspace(qt, t, d_model, d_ff, n_experts, top_k, x.device)
+    n_dev = 0 if w_gate is None else int(w_gate.shape[0])
+    n_host = 0 if w_gate_host is None else int(w_gate_host.shape[0])
+    _check(_lib.load().phb_moe_ffn_tiered(qt, _ptr(w_gate), _ptr(w_up), _ptr(w_down), n_dev,
+                                          _host_ptr(w_gate_host), _host_ptr(w_up_host), _host_ptr(w_down_host), n_host, _ptr(expert_loc), _ptr(x),
+                                          _ptr(logits), _ptr(out), t, d_model, d_ff, n_experts, top_k,
+                                          _ptr(out_idx), _ptr(out_p), _ptr(ws), ws.numel(), _stream()))
+    return out
+
 
 def prefill_workspace_size(qtype, m_tokens: int, n: int, k: int) -> int:
     return int(_lib.load().phb_gemm_q_prefill_workspace_size(qtype_id(qtype), m_tokens, n, k))

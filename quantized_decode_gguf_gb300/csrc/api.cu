@@ -231,7 +231,8 @@ phb_status phb_device_error(int* code) {
     PHB_CUDA(phb::read_dev_err_attention(&c[6]), "read device error");
     PHB_CUDA(phb::read_dev_err_gemv_xr(&c[7]), "read device error");
     *code = c[0] | c[1] | c[2] | c[3] | c[4] | c[5] | c[6] | c[7];
-    if (*code) return fail(PHB_ERR_DEVICE_TIMEOUT, "a kernel reported device error %d", *code);
+    if (*code & 1) return fail(PHB_ERR_DEVICE_TIMEOUT, "a kernel reported device error %d", *code);
+    if (*code) return fail(PHB_ERR_DEVICE_INPUT, "a kernel reported device error %d", *code);
     return ok();
 }
 
@@ -400,6 +401,111 @@ phb_status phb_moe_ffn(int qtype, const void* Wgate, const void* Wup, const void
     q.out_p = out_p;
     q.ws = ws;
     q.ws_bytes = ws_bytes;
+    const cudaError_t e = phb::moe_run(q, stream);
+    if (e == cudaErrorInvalidConfiguration) return fail(PHB_ERR_SHAPE, "shape does not fit the MoE kernels");
+    if (e != cudaSuccess) return cuda_fail(e, "moe launch");
+    return ok();
+}
+
+// ---------------------------------------------------------------- MoE with tiered experts
+size_t phb_moe_ffn_tiered_workspace_size(int qtype, int64_t n_tokens, int64_t d_model, int64_t d_ff, int n_experts,
+                                         int top_k) {
+    if (phb_moe_ffn_workspace_size(qtype, n_tokens, d_model, d_ff, n_experts, top_k) == 0) return 0;
+    phb::MoeReq q;
+    q.qt = qt_of(qtype);
+    q.t = n_tokens;
+    q.d_model = d_model;
+    q.d_ff = d_ff;
+    q.e = n_experts;
+    q.top_k = top_k;
+    static const int32_t kAnyLoc = 0;
+    q.loc = &kAnyLoc;  // any non-null table: the layout with staging slots
+    return phb::moe_ws_bytes(q);
+}
+
+// A pointer the GPU can read for the host-resident experts: pinned or
+// registered host memory (its device address), device or managed memory, or
+// any host address when the device reads pageable memory directly.
+static phb_status gpu_readable(const void* p, const void** dev) {
+    cudaPointerAttributes a{};
+    cudaError_t e = cudaPointerGetAttributes(&a, p);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes");
+    if (a.type == cudaMemoryTypeHost && a.devicePointer != nullptr) {
+        *dev = a.devicePointer;
+        return PHB_OK;
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+        *dev = p;
+        return PHB_OK;
+    }
+    int devi = 0, pageable = 0;
+    if (cudaGetDevice(&devi) == cudaSuccess &&
+        cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, devi) == cudaSuccess && pageable) {
+        *dev = p;
+        return PHB_OK;
+    }
+    return fail(PHB_ERR_INVALID_ARG, "host experts must be pinned or registered host memory the GPU can read");
+}
+
+phb_status phb_moe_ffn_tiered(int qtype, const void* Wgate, const void* Wup, const void* Wdown, int n_dev_slots,
+                              const void* Wgate_host, const void* Wup_host, const void* Wdown_host, int n_host,
+                              const int32_t* expert_loc, const float* X, const float* router_logits, float* Y,
+                              int64_t n_tokens, int64_t d_model, int64_t d_ff, int n_experts, int top_k,
+                              int32_t* out_idx, float* out_p, void* ws, size_t ws_bytes, phb_stream_t stream) {
+    const int qt = qt_of(qtype);
+    PHB_REQUIRE(qt >= 0, PHB_ERR_INVALID_ARG, "unknown qtype");
+    PHB_REQUIRE(X && router_logits && Y && expert_loc, PHB_ERR_INVALID_ARG, "null tensor pointer");
+    PHB_REQUIRE(n_dev_slots >= 0 && n_host >= 0 && n_dev_slots + n_host >= 1, PHB_ERR_INVALID_ARG,
+                "need n_dev_slots >= 0, n_host >= 0 and at least one expert copy");
+    PHB_REQUIRE(n_dev_slots == 0 || (Wgate && Wup && Wdown), PHB_ERR_INVALID_ARG, "null device expert pointer");
+    PHB_REQUIRE(n_host == 0 || (Wgate_host && Wup_host && Wdown_host), PHB_ERR_INVALID_ARG,
+                "null host expert pointer");
+    PHB_REQUIRE(n_tokens >= 1 && n_tokens <= 64, PHB_ERR_INVALID_ARG, "n_tokens must be 1..64");
+    PHB_REQUIRE(n_experts >= 1 && n_experts <= 256, PHB_ERR_INVALID_ARG, "n_experts must be 1..256");
+    PHB_REQUIRE(top_k >= 1 && top_k <= 8, PHB_ERR_INVALID_ARG, "top_k must be 1..8");
+    PHB_REQUIRE(top_k <= n_experts, PHB_ERR_SHAPE, "top_k > n_experts");
+    PHB_REQUIRE(d_model > 0 && d_ff > 0, PHB_ERR_INVALID_ARG, "d_model and d_ff must be positive");
+    PHB_REQUIRE(d_model % 256 == 0 && d_ff % 256 == 0, PHB_ERR_SHAPE, "MoE needs d_model and d_ff multiples of 256");
+    PHB_REQUIRE(d_model <= 4096 && d_ff <= 4096, PHB_ERR_SHAPE, "MoE needs d_model, d_ff <= 4096");
+    PHB_REQUIRE(aligned16(Wgate) && aligned16(Wup) && aligned16(Wdown) && aligned16(Wgate_host) &&
+                    aligned16(Wup_host) && aligned16(Wdown_host) && aligned16(X) && aligned16(router_logits) &&
+                    aligned16(Y) && aligned16(ws) && (reinterpret_cast<uintptr_t>(expert_loc) & 3u) == 0,
+                PHB_ERR_ALIGN, "tensors must be 16-byte aligned (expert_loc 4-byte)");
+    const size_t need = phb_moe_ffn_tiered_workspace_size(qtype, n_tokens, d_model, d_ff, n_experts, top_k);
+    PHB_REQUIRE(ws && ws_bytes >= need, PHB_ERR_WORKSPACE, "workspace needs %zu bytes (got %zu)", need, ws_bytes);
+    phb_status st = check_device();
+    if (st != PHB_OK) return st;
+    const void* hg = nullptr;
+    const void* hu = nullptr;
+    const void* hd = nullptr;
+    if (n_host > 0) {
+        if ((st = gpu_readable(Wgate_host, &hg)) != PHB_OK || (st = gpu_readable(Wup_host, &hu)) != PHB_OK ||
+            (st = gpu_readable(Wdown_host, &hd)) != PHB_OK)
+            return st;
+    }
+    phb::MoeReq q;
+    q.qt = qt;
+    q.wg = Wgate;
+    q.wu = Wup;
+    q.wd = Wdown;
+    q.x = X;
+    q.logits = router_logits;
+    q.y = Y;
+    q.t = n_tokens;
+    q.d_model = d_model;
+    q.d_ff = d_ff;
+    q.e = n_experts;
+    q.top_k = top_k;
+    q.out_idx = out_idx;
+    q.out_p = out_p;
+    q.ws = ws;
+    q.ws_bytes = ws_bytes;
+    q.loc = expert_loc;
+    q.n_dev_slots = n_dev_slots;
+    q.n_host = n_host;
+    q.hg = hg;
+    q.hu = hu;
+    q.hd = hd;
     const cudaError_t e = phb::moe_run(q, stream);
     if (e == cudaErrorInvalidConfiguration) return fail(PHB_ERR_SHAPE, "shape does not fit the MoE kernels");
     if (e != cudaSuccess) return cuda_fail(e, "moe launch");

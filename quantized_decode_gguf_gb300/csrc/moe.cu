@@ -18,6 +18,15 @@
 //    each 128-row tile does it (a per-tile counter in the workspace, back to
 //    zero after each call); for more tokens moe_combine_kernel.
 // All orders are fixed, so repeated calls give identical bits.
+//
+// Tiered experts (the expert cache of the README's MoE decode): when only
+// some experts fit in device memory, the caller keeps the rest in host
+// memory the GPU can read and passes a location table. After routing, a
+// fetch kernel copies every active expert that lives only in host memory
+// (read by the GPU over the host link; no CPU compute) into a device staging
+// slot and records per active slot which copy to read; the two passes then
+// take each active expert's tiles from the cache or the staging area. The
+// arithmetic is the same, so results equal the all-resident call's bit for bit.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -301,6 +310,10 @@ struct MoeRowsParams {
     int route_inline;  // gate/up pass: 1 = route in the kernel, 0 = read the routing kernel's lists
     // down pass: 1 = the last CTA of a row tile combines the slots into y_out
     int combine;
+    // tiered experts: per active slot, 1 = read the staging copy (second maps),
+    // and the expert index within the copy read (nullptr: the cache, index = expert)
+    const int32_t* src_sel;
+    const int32_t* src_z;
     int* tile_ctr;     // [row tiles], zero between calls
     float* y_out;      // Y [n_tokens][n]
 };
@@ -384,6 +397,7 @@ __device__ __forceinline__ bool moe_rows_group(const MoeRowsParams& p, const int
 template <int QT, int NMAT>
 __global__ void __launch_bounds__(kMrThreads, 1)
     moe_rows_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
+                    const __grid_constant__ CUtensorMap tm0b, const __grid_constant__ CUtensorMap tm1b,
                     const __grid_constant__ MoeRowsParams p) {
     using R = MrCfg<QT>;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -416,6 +430,10 @@ __global__ void __launch_bounds__(kMrThreads, 1)
     const int slot = blockIdx.y;
     if (slot >= n_active) return;
     const int e = act_expert[slot];
+    const bool alt = p.src_sel != nullptr && p.src_sel[slot] != 0;
+    const int z = p.src_z != nullptr ? p.src_z[slot] : e;  // expert index within the copy read
+    const CUtensorMap* m0 = alt ? &tm0b : &tm0;
+    const CUtensorMap* m1 = alt ? &tm1b : &tm1;
     const int first = act_off[slot];
     const int cnt = act_cnt[slot];
     const int64_t row0 = static_cast<int64_t>(blockIdx.x) * p.row_tile;
@@ -445,9 +463,9 @@ __global__ void __launch_bounds__(kMrThreads, 1)
                     }
                     mbar_arrive_expect_tx(&full[sl], static_cast<uint32_t>(R::stage_bytes));
                     uint8_t* dst = smem + sl * R::stage_bytes;
-                    tma_load_3d_hint(dst, &tm0, u * kElems, static_cast<int>(row0), e, &full[sl], pol);
+                    tma_load_3d_hint(dst, m0, u * kElems, static_cast<int>(row0), z, &full[sl], pol);
                     if (NMAT == 2)
-                        tma_load_3d_hint(dst + p.row_tile * R::ub, &tm1, u * kElems, static_cast<int>(row0), e,
+                        tma_load_3d_hint(dst + p.row_tile * R::ub, m1, u * kElems, static_cast<int>(row0), z,
                                          &full[sl], pol);
                     ++issued;
                 }
@@ -546,12 +564,57 @@ size_t moe_rows_layout(int qt, int64_t k, MoeRowsParams* p) {
 }
 
 template <int QT, int NMAT>
-cudaError_t launch_moe_rows(const CUtensorMap& t0, const CUtensorMap& t1, const MoeRowsParams& p, dim3 grid,
-                            size_t smem, cudaStream_t s) {
+cudaError_t launch_moe_rows(const CUtensorMap& t0, const CUtensorMap& t1, const CUtensorMap& t0b,
+                            const CUtensorMap& t1b, const MoeRowsParams& p, dim3 grid, size_t smem, cudaStream_t s) {
     constexpr auto kern = moe_rows_kernel<QT, NMAT>;
     cudaError_t e = ensure_smem_attr<kern>();
     if (e != cudaSuccess) return e;
-    return launch_kernel(kern, grid, dim3(kMrThreads), smem, s, true, t0, t1, p);
+    return launch_kernel(kern, grid, dim3(kMrThreads), smem, s, true, t0, t1, t0b, t1b, p);
+}
+
+// Tiered experts: for every active slot whose expert lives only in host
+// memory, copy its gate, up and down matrices into staging slot `slot`
+// (grid: CTAs per slot x slots; each CTA a contiguous share, 16-byte
+// accesses), and record which copy the passes read.
+__global__ void __launch_bounds__(256) moe_fetch_kernel(const int32_t* __restrict__ n_active,
+                                                        const int32_t* __restrict__ act_expert,
+                                                        const int32_t* __restrict__ loc, int n_dev, int n_host,
+                                                        const uint8_t* hg,
+                                                        const uint8_t* hu, const uint8_t* hd, uint8_t* sg, uint8_t* su,
+                                                        uint8_t* sd, int64_t bytes_gu, int64_t bytes_d,
+                                                        int32_t* src_sel, int32_t* src_z) {
+    pdl_launch_dependents();
+    pdl_wait();  // the routing comes from the previous kernel
+    const int slot = blockIdx.y;
+    if (slot >= *n_active) return;
+    const int v = loc[act_expert[slot]];
+    const int64_t h = -1 - static_cast<int64_t>(v);
+    const bool bad = v >= n_dev || (v < 0 && h >= n_host);  // neither copy exists: record it, read nothing
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        src_sel[slot] = v < 0 ? 1 : 0;
+        src_z[slot] = v < 0 ? slot : v;
+        if (bad) atomicExch(&g_dev_err, kDevErrBadIndex);
+    }
+    if (v >= 0 || bad) return;
+    auto copy = [&](const uint8_t* src, uint8_t* dst, int64_t bytes) {
+        const int64_t n16 = bytes / 16;
+        const int64_t share = (n16 + gridDim.x - 1) / gridDim.x;
+        const int64_t lo = blockIdx.x * share, hi = min(n16, lo + share);
+        const uint4* s4 = reinterpret_cast<const uint4*>(src);
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
+        int64_t i = lo + threadIdx.x;
+        for (; i + 3 * blockDim.x < hi; i += 4 * blockDim.x) {
+            const uint4 a = s4[i], b = s4[i + blockDim.x], c = s4[i + 2 * blockDim.x], d = s4[i + 3 * blockDim.x];
+            d4[i] = a;
+            d4[i + blockDim.x] = b;
+            d4[i + 2 * blockDim.x] = c;
+            d4[i + 3 * blockDim.x] = d;
+        }
+        for (; i < hi; i += blockDim.x) d4[i] = s4[i];
+    };
+    copy(hg + h * bytes_gu, sg + slot * bytes_gu, bytes_gu);
+    copy(hu + h * bytes_gu, su + slot * bytes_gu, bytes_gu);
+    copy(hd + h * bytes_d, sd + slot * bytes_d, bytes_d);
 }
 
 struct MoeWs {
@@ -559,6 +622,10 @@ struct MoeWs {
     float* h;
     float* yp;
     int* tile_ctr;  // down-pass row tiles: combine counters
+    // tiered experts only: staging copies [slots][rows][row bytes] and the per-slot source tables
+    uint8_t* stage[3];
+    int32_t* src_sel;
+    int32_t* src_z;
     size_t bytes;
 };
 
@@ -586,6 +653,16 @@ MoeWs moe_ws_layout(const MoeReq& q, void* base) {
     w.r.act_cnt = reinterpret_cast<int32_t*>(take(slots * 4));
     w.r.pair_list = reinterpret_cast<int32_t*>(take(pairs * 4));
     w.tile_ctr = reinterpret_cast<int*>(take(static_cast<size_t>((q.d_model + kMrRows - 1) / kMrRows) * 4));
+    if (q.loc != nullptr) {
+        const int ub = q.qt == 0 ? Fmt<0>::unit_bytes : Fmt<1>::unit_bytes;
+        const size_t gu = static_cast<size_t>(q.d_ff) * (q.d_model / kUnitWeights) * ub;
+        const size_t dn = static_cast<size_t>(q.d_model) * (q.d_ff / kUnitWeights) * ub;
+        w.src_sel = reinterpret_cast<int32_t*>(take(slots * 4));
+        w.src_z = reinterpret_cast<int32_t*>(take(slots * 4));
+        w.stage[0] = take(slots * gu);
+        w.stage[1] = take(slots * gu);
+        w.stage[2] = take(slots * dn);
+    }
     w.bytes = off;
     return w;
 }
@@ -605,7 +682,9 @@ cudaError_t moe_run(const MoeReq& q, cudaStream_t s) {
     const int pairs = static_cast<int>(q.t * q.top_k);
     const int slots = std::min(q.e, pairs);
     cudaError_t e;
-    const bool inline_route = q.t <= kMoeInlineRouteTokens;
+    const bool tiered = q.loc != nullptr;
+    // tiered experts route in their own kernel: the fetch kernel needs the list first
+    const bool inline_route = q.t <= kMoeInlineRouteTokens && !tiered;
     if (!inline_route) {
         e = launch_kernel(moe_route_kernel, dim3(1), dim3(256), 0, s, true, q.logits, static_cast<int>(q.t), q.e,
                           q.top_k, w.r, q.out_idx, q.out_p);
@@ -613,11 +692,36 @@ cudaError_t moe_run(const MoeReq& q, cudaStream_t s) {
     }
     // row-resident grouped passes (3-D TMA unit stages)
     {
-        CUtensorMap tg, tu, td;
-        if (!encode_expert_map(&tg, q.qt, q.wg, q.e, q.d_ff, q.d_model, 64) ||
-            !encode_expert_map(&tu, q.qt, q.wu, q.e, q.d_ff, q.d_model, 64) ||
-            !encode_expert_map(&td, q.qt, q.wd, q.e, q.d_model, q.d_ff, kMrRows))
+        // experts in the arrays wg, wu, wd (a tiered call without a device cache maps the staging area there)
+        const bool no_cache = tiered && q.n_dev_slots == 0;
+        const int n_cache = no_cache ? slots : tiered ? q.n_dev_slots : q.e;
+        const void* cg = no_cache ? w.stage[0] : q.wg;
+        const void* cu = no_cache ? w.stage[1] : q.wu;
+        const void* cd = no_cache ? w.stage[2] : q.wd;
+        CUtensorMap tg, tu, td, sg, su, sd;
+        if (!encode_expert_map(&tg, q.qt, cg, n_cache, q.d_ff, q.d_model, 64) ||
+            !encode_expert_map(&tu, q.qt, cu, n_cache, q.d_ff, q.d_model, 64) ||
+            !encode_expert_map(&td, q.qt, cd, n_cache, q.d_model, q.d_ff, kMrRows))
             return cudaErrorInvalidValue;
+        sg = tg;
+        su = tu;
+        sd = td;
+        if (tiered) {
+            if (!encode_expert_map(&sg, q.qt, w.stage[0], slots, q.d_ff, q.d_model, 64) ||
+                !encode_expert_map(&su, q.qt, w.stage[1], slots, q.d_ff, q.d_model, 64) ||
+                !encode_expert_map(&sd, q.qt, w.stage[2], slots, q.d_model, q.d_ff, kMrRows))
+                return cudaErrorInvalidValue;
+            const int ub = q.qt == 0 ? Fmt<0>::unit_bytes : Fmt<1>::unit_bytes;
+            const int64_t gu = q.d_ff * (q.d_model / kUnitWeights) * ub;
+            const int64_t dn = q.d_model * (q.d_ff / kUnitWeights) * ub;
+            e = launch_kernel(moe_fetch_kernel, dim3(32, static_cast<unsigned>(slots)), dim3(256), 0, s, true,
+                              static_cast<const int32_t*>(w.r.n_active), static_cast<const int32_t*>(w.r.act_expert),
+                              q.loc, q.n_dev_slots, q.n_host, static_cast<const uint8_t*>(q.hg),
+                              static_cast<const uint8_t*>(q.hu),
+                              static_cast<const uint8_t*>(q.hd), w.stage[0], w.stage[1], w.stage[2], gu, dn,
+                              w.src_sel, w.src_z);
+            if (e != cudaSuccess) return e;
+        }
         MoeRowsParams pg{};
         const size_t smem_g = moe_rows_layout(q.qt, q.d_model, &pg);
         pg.x = q.x;
@@ -637,9 +741,12 @@ cudaError_t moe_run(const MoeReq& q, cudaStream_t s) {
         pg.out_idx = q.out_idx;
         pg.out_p = q.out_p;
         pg.route_inline = inline_route ? 1 : 0;
+        pg.src_sel = tiered ? w.src_sel : nullptr;
+        pg.src_z = tiered ? w.src_z : nullptr;
         if (smem_g > kSmemOptin) return cudaErrorInvalidConfiguration;
         const dim3 gg(static_cast<unsigned>(cdiv(q.d_ff, 64)), static_cast<unsigned>(slots));
-        e = q.qt == 0 ? launch_moe_rows<0, 2>(tg, tu, pg, gg, smem_g, s) : launch_moe_rows<1, 2>(tg, tu, pg, gg, smem_g, s);
+        e = q.qt == 0 ? launch_moe_rows<0, 2>(tg, tu, sg, su, pg, gg, smem_g, s)
+                      : launch_moe_rows<1, 2>(tg, tu, sg, su, pg, gg, smem_g, s);
         if (e != cudaSuccess) return e;
         MoeRowsParams pd{};
         const size_t smem_d = moe_rows_layout(q.qt, q.d_ff, &pd);
@@ -654,13 +761,17 @@ cudaError_t moe_run(const MoeReq& q, cudaStream_t s) {
         pd.units_row = static_cast<int>(q.d_ff / kUnitWeights);
         pd.row_tile = kMrRows;
         pd.trace_id = tb + 2;
-        pd.combine = inline_route ? 1 : 0;  // one or two tokens: the combine is a few loads per output
+        // one or two tokens: the combine is a few loads per output, done by the down pass
+        pd.combine = q.t <= kMoeInlineRouteTokens ? 1 : 0;
+        pd.src_sel = tiered ? w.src_sel : nullptr;
+        pd.src_z = tiered ? w.src_z : nullptr;
         pd.tile_ctr = w.tile_ctr;
         pd.y_out = q.y;
         pd.n_tokens = static_cast<int>(q.t);
         if (smem_d > kSmemOptin) return cudaErrorInvalidConfiguration;
         const dim3 gd(static_cast<unsigned>(cdiv(q.d_model, kMrRows)), static_cast<unsigned>(slots));
-        e = q.qt == 0 ? launch_moe_rows<0, 1>(td, td, pd, gd, smem_d, s) : launch_moe_rows<1, 1>(td, td, pd, gd, smem_d, s);
+        e = q.qt == 0 ? launch_moe_rows<0, 1>(td, td, sd, sd, pd, gd, smem_d, s)
+                      : launch_moe_rows<1, 1>(td, td, sd, sd, pd, gd, smem_d, s);
         if (e != cudaSuccess || pd.combine) return e;
         const int64_t total = q.t * q.d_model;
         return launch_kernel(moe_combine_kernel, dim3(static_cast<unsigned>(cdiv(total, 256))), dim3(256), 0, s, true,

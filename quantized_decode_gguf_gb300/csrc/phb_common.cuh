@@ -24,7 +24,8 @@ template <> struct Fmt<0> { static constexpr int unit_bytes = 272; };  // Q8_0
 template <> struct Fmt<1> { static constexpr int unit_bytes = 144; };  // Q4_K
 
 // Device error codes written to a kernel's error word.
-constexpr int kDevErrTimeout = 1;
+constexpr int kDevErrTimeout = 1;   // a bounded wait ran out
+constexpr int kDevErrBadIndex = 2;  // an input index (a tiered expert's location) was out of range
 
 // Upper bound on mbarrier polls before a wait is declared stuck (the wall
 // clock bound kWaitLimitNs below normally ends a stuck wait first).

@@ -132,6 +132,14 @@ struct MoeReq {
     float* out_p = nullptr;
     void* ws = nullptr;
     size_t ws_bytes = 0;
+    // tiered experts (nullptr loc: every expert is in wg/wu/wd, indexed by expert):
+    // loc[e] >= 0: expert e is slot loc[e] of the device arrays wg/wu/wd (n_dev_slots experts);
+    // loc[e] < 0: expert e is entry -1 - loc[e] of the GPU-readable host arrays hg/hu/hd
+    const int32_t* loc = nullptr;
+    int n_dev_slots = 0, n_host = 0;
+    const void* hg = nullptr;
+    const void* hu = nullptr;
+    const void* hd = nullptr;
 };
 size_t moe_ws_bytes(const MoeReq& q);
 cudaError_t moe_run(const MoeReq& q, cudaStream_t s);

@@ -150,3 +150,22 @@ def test_ffn_noalloc_rejects_bad_arguments_without_a_device(lib):
     assert f(12, FAKE, FAKE, FAKE, FAKE, FAKE, 2048, 768 + 32, 1, None) == SHAPE
     assert f(8, FAKE, FAKE, FAKE, FAKE, FAKE, 2048, 768, 0, None) == INVALID
     assert f(12, FAKE, FAKE, FAKE, FAKE, FAKE, 8192, 28672, 8, None) == WORKSPACE and "scratch" in _err(lib)
+
+
+def test_moe_tiered_rejects_bad_arguments(lib):
+    m = lib.phb_moe_ffn_tiered
+    dev = [FAKE, FAKE, FAKE]
+    host = [FAKE, FAKE, FAKE]
+    tail = [FAKE, FAKE, FAKE, 1, 2048, 768, 128, 8, None, None, FAKE, 1 << 34, None]
+    assert m(12, *dev, 0, *host, 0, FAKE, *tail) == INVALID            # no expert copy at all
+    assert m(12, *dev, 64, *host, 64, None, *tail) == INVALID          # no location table
+    assert m(12, None, FAKE, FAKE, 64, *host, 64, FAKE, *tail) == INVALID
+    assert m(12, *dev, 64, None, FAKE, FAKE, 64, FAKE, *tail) == INVALID
+    assert m(12, *dev, 64, *host, 64, FAKE + 2, *tail) == ALIGN
+    assert m(12, *dev, 64, *host, 64, FAKE, FAKE, FAKE, FAKE, 1, 2048 + 32, 768, 128, 8, None, None, FAKE,
+             1 << 34, None) == SHAPE
+    assert m(12, *dev, 64, *host, 64, FAKE, *tail[:-3], FAKE, 64, None) == WORKSPACE
+    plain = lib.phb_moe_ffn_workspace_size(12, 16, 2048, 768, 128, 8)
+    tiered = lib.phb_moe_ffn_tiered_workspace_size(12, 16, 2048, 768, 128, 8)
+    # the tiered workspace adds one staging slot per possible active expert (min(E, T*k) = 128)
+    assert tiered >= plain + 128 * (2 * 768 * 1152 + 2048 * 432)
