@@ -572,6 +572,8 @@ cudaError_t launch_moe_rows(const CUtensorMap& t0, const CUtensorMap& t1, const 
     return launch_kernel(kern, grid, dim3(kMrThreads), smem, s, true, t0, t1, t0b, t1b, p);
 }
 
+constexpr int kFetchCtas = 96;  // CTAs per active slot of the fetch kernel
+
 // Tiered experts: for every active slot whose expert lives only in host
 // memory, copy its gate, up and down matrices into staging slot `slot`
 // (grid: CTAs per slot x slots; each CTA a contiguous share, 16-byte
@@ -602,13 +604,14 @@ __global__ void __launch_bounds__(256) moe_fetch_kernel(const int32_t* __restric
         const int64_t lo = blockIdx.x * share, hi = min(n16, lo + share);
         const uint4* s4 = reinterpret_cast<const uint4*>(src);
         uint4* d4 = reinterpret_cast<uint4*>(dst);
+        constexpr int kInFlight = 8;  // 16-byte reads in flight per thread: the host link's latency is long
         int64_t i = lo + threadIdx.x;
-        for (; i + 3 * blockDim.x < hi; i += 4 * blockDim.x) {
-            const uint4 a = s4[i], b = s4[i + blockDim.x], c = s4[i + 2 * blockDim.x], d = s4[i + 3 * blockDim.x];
-            d4[i] = a;
-            d4[i + blockDim.x] = b;
-            d4[i + 2 * blockDim.x] = c;
-            d4[i + 3 * blockDim.x] = d;
+        for (; i + (kInFlight - 1) * blockDim.x < hi; i += kInFlight * blockDim.x) {
+            uint4 v[kInFlight];
+#pragma unroll
+            for (int u = 0; u < kInFlight; ++u) v[u] = s4[i + u * blockDim.x];
+#pragma unroll
+            for (int u = 0; u < kInFlight; ++u) d4[i + u * blockDim.x] = v[u];
         }
         for (; i < hi; i += blockDim.x) d4[i] = s4[i];
     };
@@ -714,7 +717,8 @@ cudaError_t moe_run(const MoeReq& q, cudaStream_t s) {
             const int ub = q.qt == 0 ? Fmt<0>::unit_bytes : Fmt<1>::unit_bytes;
             const int64_t gu = q.d_ff * (q.d_model / kUnitWeights) * ub;
             const int64_t dn = q.d_model * (q.d_ff / kUnitWeights) * ub;
-            e = launch_kernel(moe_fetch_kernel, dim3(32, static_cast<unsigned>(slots)), dim3(256), 0, s, true,
+            // enough CTAs per active expert to keep many host reads in flight
+            e = launch_kernel(moe_fetch_kernel, dim3(kFetchCtas, static_cast<unsigned>(slots)), dim3(256), 0, s, true,
                               static_cast<const int32_t*>(w.r.n_active), static_cast<const int32_t*>(w.r.act_expert),
                               q.loc, q.n_dev_slots, q.n_host, static_cast<const uint8_t*>(q.hg),
                               static_cast<const uint8_t*>(q.hu),
