@@ -102,7 +102,12 @@ def test_gemv_extreme_activation_magnitudes(qtype):
     y = to_host(phb.gemv(qtype, to_dev(blob), to_dev(x), n, k))
     ref, s = oracle.gemv_quant(qtype, blob, x, n, k)
     assert np.all(np.isfinite(y))
-    assert_within(y, ref, 1e-3 * s + 1e-44, f"gemv {qtype} extreme magnitudes")
+    # Below 2^-126 an fp32 result is a subnormal, spaced 2^-149 apart: scaling a
+    # 128-weight partial sum back into fp32 may round it by up to half that
+    # spacing, 2^-150, once per partial (k / 128 of them), and so may the
+    # result itself; relative error bounds say nothing there.
+    quantum = (k // 128 + 1) * 2.0 ** -150
+    assert_within(y, ref, 1e-3 * s + quantum, f"gemv {qtype} extreme magnitudes")
     assert np.all(y[2] == 0.0)
     check_device_clean()
 
