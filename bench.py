@@ -386,9 +386,9 @@ def bench_prefill(qtype, n, k, m, iters, seed, peaks):
 ATTN_SHAPE = (16, 4, 128)  # query heads, KV heads, head size of the dense decode workload
 
 
-def attention_inputs(n_ctx, seed):
+def attention_inputs(n_ctx, seed, hd=ATTN_SHAPE[2]):
     import torch
-    n_q, n_kv, hd = ATTN_SHAPE
+    n_q, n_kv = ATTN_SHAPE[0], ATTN_SHAPE[1]
     q = torch.from_numpy(synth.normal_f32(seed, 0, (n_q, hd))).cuda()
     k = torch.from_numpy(synth.normal_f16(seed, 1, (n_ctx, n_kv, hd))).cuda()
     v = torch.from_numpy(synth.normal_f16(seed, 2, (n_ctx, n_kv, hd))).cuda()
@@ -525,21 +525,48 @@ def run_profile(args):
             for l in range(n_layers):
                 phb.moe_ffn("q4_k", *mats[l], x, logits[l], d_model, d_ff, e, top_k, out=y, ws=ws)
         what = f"MoE FFN Q4_K, {t_tokens} tokens, {n_layers} layers"
+    elif args.profile == "dequant":
+        qt, n, k, _ = args.gemv.split(",")
+        n, k = int(n), int(k)
+        w = torch.from_numpy(synth.blocks(qt, seed, 0, n, k)).cuda()
+        out = torch.empty((n, k), device="cuda")
+        call = lambda: phb.dequant(qt, w, n, k, out=out)  # noqa: E731
+        what = f"dequant {qt} {n}x{k} to fp32"
+    elif args.profile == "moe-tiered":
+        e, top_k, d_model, d_ff, t_tokens = 128, 8, 2048, 768, 1
+        rb_in, rb_ff = row_bytes("q4_k", d_model), row_bytes("q4_k", d_ff)
+        gu = synth.q4_k_blocks(seed, 2000, 2 * e * d_ff, d_model).reshape(2, e, d_ff, rb_in)
+        dn = synth.q4_k_blocks(seed, 3000, e * d_model, d_ff).reshape(e, d_model, rb_ff)
+        res, host = np.arange(0, e, 2), np.arange(1, e, 2)
+        loc = np.empty(e, dtype=np.int32)
+        loc[res] = np.arange(len(res), dtype=np.int32)
+        loc[host] = -1 - np.arange(len(host), dtype=np.int32)
+        dev = tuple(torch.from_numpy(np.ascontiguousarray(m[res])).cuda() for m in (gu[0], gu[1], dn))
+        hst = tuple(torch.from_numpy(np.ascontiguousarray(m[host])).pin_memory() for m in (gu[0], gu[1], dn))
+        loc_d = torch.from_numpy(loc).cuda()
+        x = torch.from_numpy(synth.normal_f32(seed, 1, (t_tokens, d_model))).cuda()
+        lg = torch.from_numpy(synth.normal_f32(seed, 5000, (t_tokens, e))).cuda()
+        y = torch.empty_like(x)
+        ws = phb.moe_tiered_workspace("q4_k", t_tokens, d_model, d_ff, e, top_k)
+        call = lambda: phb.moe_ffn_tiered("q4_k", *dev, *hst, loc_d, x, lg, d_model, d_ff, e, top_k,  # noqa: E731
+                                          out=y, ws=ws)
+        what = "MoE FFN Q4_K with tiered experts, half in pinned host memory, one token, one layer"
     elif args.profile == "attention":
-        n_q, n_kv, hd = ATTN_SHAPE
-        q, k, v = attention_inputs(args.ctx, seed)
+        n_q, n_kv, hd = ATTN_SHAPE[0], ATTN_SHAPE[1], args.hd
+        q, k, v = attention_inputs(args.ctx, seed, hd)
         out = torch.empty((n_q, hd), device="cuda")
         ws = phb.workspace(phb.attention_workspace_size(args.ctx, n_q, n_kv, hd))
         call = lambda: phb.attention_decode(q, k, v, args.ctx, n_q, n_kv, hd, out=out, ws=ws)  # noqa: E731
         what = f"decode attention, {args.ctx} positions, {n_q}q/{n_kv}kv x {hd}"
     else:
-        n, k, m = 9728, 2560, 512
-        w = torch.from_numpy(synth.blocks("q4_k", seed, 0, n, k)).cuda()
+        qt, n, k = args.prefill.split(",")
+        n, k, m = int(n), int(k), 512
+        w = torch.from_numpy(synth.blocks(qt, seed, 0, n, k)).cuda()
         x = torch.from_numpy(synth.normal_f32(seed, 1, (m, k))).cuda()
         y = torch.empty((m, n), device="cuda")
-        ws = phb.workspace(phb.prefill_workspace_size("q4_k", m, n, k))
-        call = lambda: phb.gemm_q_prefill("q4_k", w, x, n, k, out=y, ws=ws)  # noqa: E731
-        what = f"prefill GEMM Q4_K {m}x{n}x{k}"
+        ws = phb.workspace(phb.prefill_workspace_size(qt, m, n, k))
+        call = lambda: phb.gemm_q_prefill(qt, w, x, n, k, out=y, ws=ws)  # noqa: E731
+        what = f"prefill GEMM {qt} {m}x{n}x{k}"
     for _ in range(args.warmup + args.steps):
         call()
     torch.cuda.synchronize()
@@ -559,12 +586,15 @@ def main():
     ap.add_argument("--impl", default="phb", choices=["phb", "reference"])
     ap.add_argument("--headline-only", action="store_true", help="skip the extra rows")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["decode", "decode-unfused", "prefill", "moe1", "moe16", "gemv", "attention"],
+    ap.add_argument("--profile", choices=["decode", "decode-unfused", "prefill", "moe1", "moe16", "gemv", "attention",
+                                          "dequant", "moe-tiered"],
                     help="run only this path --steps times after --warmup calls (a small case for ncu) and print "
                          "one status line instead of the bench line")
     ap.add_argument("--layers", type=int, default=N_LAYERS, help="decode layers in --profile decode modes")
     ap.add_argument("--gemv", default="q4_k,9728,2560,4", help="--profile gemv case: qtype,n,k,batch")
     ap.add_argument("--ctx", type=int, default=32768, help="--profile attention: context positions")
+    ap.add_argument("--hd", type=int, default=128, help="--profile attention: head dim")
+    ap.add_argument("--prefill", default="q4_k,9728,2560", help="--profile prefill case: qtype,n,k (512 tokens)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
