@@ -125,8 +125,10 @@ __device__ __forceinline__ void dot_q8_0_half(const uint8_t* wsrc, const float* 
 
 // dot_q8_0_half for one activation row held in registers: xr the half
 // unit's 128 scaled activations. A thread that keeps xr across many rows
-// reads only weights from shared memory. Same arithmetic, in the same order,
-// as dot_q8_0_half with MAXB = 1; returns the scaled-back sum.
+// reads only weights from shared memory. The same exact scaled weights as
+// dot_q8_0_half, summed in two interleaved accumulators (weights 4i, 4i+1
+// and 4i+2, 4i+3) so that consecutive fused multiply-adds do not wait on
+// each other; returns the scaled-back sum.
 __device__ __forceinline__ float dot_q8_0_half_xr(const uint8_t* wsrc, const float (&xr)[128], float xfac) {
     uint32_t wd[34];
 #pragma unroll
@@ -135,7 +137,7 @@ __device__ __forceinline__ float dot_q8_0_half_xr(const uint8_t* wsrc, const flo
         wd[2 * i] = v.x;
         wd[2 * i + 1] = v.y;
     }
-    float2 s2 = make_float2(0.f, 0.f);
+    float2 s2 = make_float2(0.f, 0.f), t2 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int bb = 0; bb < 4; ++bb) {
         const int ob = 34 * bb;
@@ -151,10 +153,10 @@ __device__ __forceinline__ float dot_q8_0_half_xr(const uint8_t* wsrc, const flo
             }
             const int k = 32 * bb + 4 * i4;
             s2 = __ffma2_rn(wpair(a, u[0], u[1], c), make_float2(xr[k], xr[k + 1]), s2);
-            s2 = __ffma2_rn(wpair(a, u[2], u[3], c), make_float2(xr[k + 2], xr[k + 3]), s2);
+            t2 = __ffma2_rn(wpair(a, u[2], u[3], c), make_float2(xr[k + 2], xr[k + 3]), t2);
         }
     }
-    return (s2.x + s2.y) * xfac;
+    return ((s2.x + s2.y) + (t2.x + t2.y)) * xfac;
 }
 
 // 6-bit scale and min of sub-block 4h + jj from the 12 scale bytes (packed
@@ -249,7 +251,8 @@ __device__ __forceinline__ void dot_q4_k_half(const uint8_t* blk, int h, const f
 }
 
 // dot_q4_k_half for one activation row held in registers (see
-// dot_q8_0_half_xr); same arithmetic, in the same order, as MAXB = 1.
+// dot_q8_0_half_xr): the same exact scaled weights, the low-nibble and the
+// high-nibble terms summed in two accumulators.
 __device__ __forceinline__ float dot_q4_k_half_xr(const uint8_t* blk, int h, const float (&xr)[128], float xfac) {
     const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
     float a[4], c[4];
@@ -263,7 +266,7 @@ __device__ __forceinline__ float dot_q4_k_half_xr(const uint8_t* blk, int h, con
         qw[4 * i + 2] = v.z;
         qw[4 * i + 3] = v.w;
     }
-    float2 s2 = make_float2(0.f, 0.f);
+    float2 s2 = make_float2(0.f, 0.f), t2 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc) {
         const float al = a[2 * cc], cl = c[2 * cc], ah = a[2 * cc + 1] * 0.0625f, ch = c[2 * cc + 1];
@@ -275,11 +278,11 @@ __device__ __forceinline__ float dot_q4_k_half_xr(const uint8_t* blk, int h, con
             const int kl = 64 * cc + 4 * wi, kh = kl + 32;
             s2 = __ffma2_rn(wpair(al, byte_subnormal<0>(lo), byte_subnormal<1>(lo), cl), make_float2(xr[kl], xr[kl + 1]), s2);
             s2 = __ffma2_rn(wpair(al, byte_subnormal<2>(lo), byte_subnormal<3>(lo), cl), make_float2(xr[kl + 2], xr[kl + 3]), s2);
-            s2 = __ffma2_rn(wpair(ah, byte_subnormal<0>(hi), byte_subnormal<1>(hi), ch), make_float2(xr[kh], xr[kh + 1]), s2);
-            s2 = __ffma2_rn(wpair(ah, byte_subnormal<2>(hi), byte_subnormal<3>(hi), ch), make_float2(xr[kh + 2], xr[kh + 3]), s2);
+            t2 = __ffma2_rn(wpair(ah, byte_subnormal<0>(hi), byte_subnormal<1>(hi), ch), make_float2(xr[kh], xr[kh + 1]), t2);
+            t2 = __ffma2_rn(wpair(ah, byte_subnormal<2>(hi), byte_subnormal<3>(hi), ch), make_float2(xr[kh + 2], xr[kh + 3]), t2);
         }
     }
-    return (s2.x + s2.y) * xfac;
+    return ((s2.x + s2.y) + (t2.x + t2.y)) * xfac;
 }
 
 }  // namespace phb

@@ -297,6 +297,34 @@ __device__ __forceinline__ int pick_scale_exp(float amax) {
     return min(kWShift + 126, 125 - e);
 }
 
+// Register-resident activations: copy the 128 values of one half unit from
+// shared memory (padded layout, 16-byte aligned) into xr, scaled by 2^s with
+// s picked from their own largest magnitude, and return the factor
+// 2^(kWShift - s) that takes a half-unit dot back to the true scale.
+__device__ __forceinline__ float load_xr_scaled(const float* xp, float (&xr)[128]) {
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const float4 v = *reinterpret_cast<const float4*>(xp + 4 * i);
+        xr[4 * i] = v.x;
+        xr[4 * i + 1] = v.y;
+        xr[4 * i + 2] = v.z;
+        xr[4 * i + 3] = v.w;
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
+    const int se = pick_scale_exp(amax);
+    const int e1 = min(se, 127);
+    const float f1 = __int_as_float((e1 + 127) << 23);
+#pragma unroll
+    for (int i = 0; i < 128; ++i) xr[i] *= f1;
+    if (se > 127) {  // largest magnitude below 2^-3: the rest of the power of two
+        const float f2 = __int_as_float((se - e1 + 127) << 23);
+#pragma unroll
+        for (int i = 0; i < 128; ++i) xr[i] *= f2;
+    }
+    return __int_as_float((kWShift - se + 127) << 23);
+}
+
 template <int CW, int MAXB, int XMODE>
 __device__ __forceinline__ void stage_x(const float* x, int64_t ldx, int64_t kbase, int kseg, int batch, float* xs,
                                        float* xfac, float* red, int gather_group, int gather_hd,

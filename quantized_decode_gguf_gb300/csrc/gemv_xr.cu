@@ -120,30 +120,7 @@ __global__ void __launch_bounds__(32 * CW + 32, CW <= 6 ? 2 : 1) gemv_xr_kernel(
     consumer_sync<C::consumers>();
     float xr[128];
     float xf = 1.f;
-    if (active) {
-        const float* xp = xs + pos * (kXPadEvery + kXPad);
-        float amax = 0.f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const float4 v = *reinterpret_cast<const float4*>(xp + 4 * i);
-            xr[4 * i] = v.x;
-            xr[4 * i + 1] = v.y;
-            xr[4 * i + 2] = v.z;
-            xr[4 * i + 3] = v.w;
-            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-        }
-        const int se = pick_scale_exp(amax);
-        const int e1 = min(se, 127);
-        const float f1 = __int_as_float((e1 + 127) << 23);
-#pragma unroll
-        for (int i = 0; i < 128; ++i) xr[i] *= f1;
-        if (se > 127) {  // largest magnitude below 2^-3: the rest of the power of two
-            const float f2 = __int_as_float((se - e1 + 127) << 23);
-#pragma unroll
-            for (int i = 0; i < 128; ++i) xr[i] *= f2;
-        }
-        xf = __int_as_float((kWShift - se + 127) << 23);
-    }
+    if (active) xf = load_xr_scaled(xs + pos * (kXPadEvery + kXPad), xr);
     if (tid == 0) PHB_TRACE_EV(p.trace_id, 2);
 
     const int nseg = NMAT * t.rows_here;
