@@ -221,7 +221,7 @@ phb_status phb_device_error(int* code) {
     phb_status st = check_device();
     if (st != PHB_OK) return st;
     PHB_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
-    int c[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    int c[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
     PHB_CUDA(phb::read_dev_err_gemv(&c[0]), "read device error");
     PHB_CUDA(phb::read_dev_err_decode(&c[1]), "read device error");
     PHB_CUDA(phb::read_dev_err_moe(&c[2]), "read device error");
@@ -230,7 +230,9 @@ phb_status phb_device_error(int* code) {
     PHB_CUDA(phb::read_dev_err_gemv_rows(&c[5]), "read device error");
     PHB_CUDA(phb::read_dev_err_attention(&c[6]), "read device error");
     PHB_CUDA(phb::read_dev_err_gemv_xr(&c[7]), "read device error");
-    *code = c[0] | c[1] | c[2] | c[3] | c[4] | c[5] | c[6] | c[7];
+    PHB_CUDA(phb::read_dev_err_moe_token(&c[8]), "read device error");
+    *code = 0;
+    for (int v : c) *code |= v;
     if (*code & 1) return fail(PHB_ERR_DEVICE_TIMEOUT, "a kernel reported device error %d", *code);
     if (*code) return fail(PHB_ERR_DEVICE_INPUT, "a kernel reported device error %d", *code);
     return ok();

@@ -36,6 +36,7 @@
 #include <mutex>
 
 #include "gemv_plan.cuh"
+#include "moe_route.cuh"
 #include "phb_internal.h"
 
 namespace phb {
@@ -59,8 +60,6 @@ extern "C" int phb_trace_read_moe(void* dst, size_t bytes) {
 
 namespace {
 
-constexpr int kMaxExperts = 256;
-constexpr int kMaxTopK = 8;
 constexpr int kMaxTokens = 64;
 // Tokens per pass over a staged weight tile. Four keeps the staged
 // activations small enough for two CTAs per SM; an expert chosen by more
@@ -78,16 +77,6 @@ struct RouteOut {
     int32_t* pair_list;  // [T*k]
 };
 
-// Order-preserving map of a finite float to an unsigned key (larger float,
-// larger key).
-__device__ __forceinline__ uint32_t float_key(float v) {
-    const uint32_t u = __float_as_uint(v);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-__device__ __forceinline__ float key_float(uint32_t k) {
-    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
-}
 
 // Routing state in shared memory.
 struct RouteSm {
@@ -101,6 +90,7 @@ struct RouteSm {
     int32_t pair_list[kMaxTokens * kMaxTopK];
     int32_t n_active;
 };
+
 
 // Routing by 256 threads (the CTA's consumers; named barrier 1). Warps take
 // tokens; per token, K rounds of a warp-wide arg-max (largest logit, then
@@ -116,56 +106,20 @@ __device__ __forceinline__ void route_block(const float* __restrict__ logits, in
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     for (int e = tid; e < kMaxExperts; e += NT) sm->cnt[e] = 0;
     for (int t = warp; t < T; t += NT / 32) {
-        uint32_t key[kMaxExperts / 32];
-#pragma unroll
-        for (int j = 0; j < kMaxExperts / 32; ++j) {
-            const int e = lane + 32 * j;
-            key[j] = e < E ? float_key(logits[static_cast<int64_t>(t) * E + e]) : 0u;
-        }
-        uint32_t taken = 0;
-        float sel_v[kMaxTopK];
         int sel_e[kMaxTopK];
-#pragma unroll
-        for (int r = 0; r < kMaxTopK; ++r) {
-            if (r >= K) break;
-            // this lane's best untaken expert: largest key, then lowest index (ascending j)
-            uint32_t bk = 0;
-            int be = 0x7FFFFFFF;
-#pragma unroll
-            for (int j = 0; j < kMaxExperts / 32; ++j) {
-                const int e = lane + 32 * j;
-                if (e < E && !((taken >> j) & 1u) && (be == 0x7FFFFFFF || key[j] > bk)) {
-                    bk = key[j];
-                    be = e;
-                }
-            }
-            const uint32_t kmax = __reduce_max_sync(0xFFFFFFFFu, bk);
-            const uint32_t emin = __reduce_min_sync(0xFFFFFFFFu, (be != 0x7FFFFFFF && bk == kmax)
-                                                                     ? static_cast<uint32_t>(be) : 0xFFFFFFFFu);
-            if (static_cast<int>(emin & 31u) == lane) taken |= 1u << (emin >> 5);
-            sel_v[r] = key_float(kmax);
-            sel_e[r] = static_cast<int>(emin);
-        }
+        float pr[kMaxTopK];
+        route_token_warp(logits + static_cast<int64_t>(t) * E, E, K, lane, sel_e, pr);
         if (lane == 0) {
-            float ex[kMaxTopK];
-            float sum = 0.f;
 #pragma unroll
             for (int r = 0; r < kMaxTopK; ++r) {
                 if (r >= K) break;
-                ex[r] = expf(sel_v[r] - sel_v[0]);
-                sum += ex[r];
-            }
-#pragma unroll
-            for (int r = 0; r < kMaxTopK; ++r) {
-                if (r >= K) break;
-                const float pr = ex[r] / sum;
                 const int q = t * K + r;
                 sm->sidx[q] = sel_e[r];
                 if (go) {
                     go->idx[q] = sel_e[r];
-                    go->p[q] = pr;
+                    go->p[q] = pr[r];
                     if (out_idx) out_idx[q] = sel_e[r];
-                    if (out_p) out_p[q] = pr;
+                    if (out_p) out_p[q] = pr[r];
                 }
             }
         }
@@ -625,6 +579,9 @@ struct MoeWs {
     float* h;
     float* yp;
     int* tile_ctr;  // down-pass row tiles: combine counters
+    // one token: the one-token kernel's tagged h replicas and its call epoch
+    uint2* tok_hx;
+    unsigned* tok_epoch;
     // tiered experts only: staging copies [slots][rows][row bytes] and the per-slot source tables
     uint8_t* stage[3];
     int32_t* src_sel;
@@ -656,6 +613,10 @@ MoeWs moe_ws_layout(const MoeReq& q, void* base) {
     w.r.act_cnt = reinterpret_cast<int32_t*>(take(slots * 4));
     w.r.pair_list = reinterpret_cast<int32_t*>(take(pairs * 4));
     w.tile_ctr = reinterpret_cast<int*>(take(static_cast<size_t>((q.d_model + kMrRows - 1) / kMrRows) * 4));
+    if (q.t == 1) {
+        w.tok_epoch = reinterpret_cast<unsigned*>(take(16));
+        w.tok_hx = reinterpret_cast<uint2*>(take(static_cast<size_t>(kTokReplicas) * q.top_k * q.d_ff * 8));
+    }
     if (q.loc != nullptr) {
         const int ub = q.qt == 0 ? Fmt<0>::unit_bytes : Fmt<1>::unit_bytes;
         const size_t gu = static_cast<size_t>(q.d_ff) * (q.d_model / kUnitWeights) * ub;
@@ -686,12 +647,40 @@ cudaError_t moe_run(const MoeReq& q, cudaStream_t s) {
     const int slots = std::min(q.e, pairs);
     cudaError_t e;
     const bool tiered = q.loc != nullptr;
+    // one token: one cooperative kernel over all SMs (moe_token.cu) where the shape fits
+    const bool token = q.t == 1 && moe_token_fits(q);
     // tiered experts route in their own kernel: the fetch kernel needs the list first
     const bool inline_route = q.t <= kMoeInlineRouteTokens && !tiered;
     if (!inline_route) {
         e = launch_kernel(moe_route_kernel, dim3(1), dim3(256), 0, s, true, q.logits, static_cast<int>(q.t), q.e,
                           q.top_k, w.r, q.out_idx, q.out_p);
         if (e != cudaSuccess) return e;
+    }
+    if (tiered) {
+        const int ub = q.qt == 0 ? Fmt<0>::unit_bytes : Fmt<1>::unit_bytes;
+        const int64_t gu = q.d_ff * (q.d_model / kUnitWeights) * ub;
+        const int64_t dn = q.d_model * (q.d_ff / kUnitWeights) * ub;
+        // enough CTAs per active expert to keep many host reads in flight
+        e = launch_kernel(moe_fetch_kernel, dim3(kFetchCtas, static_cast<unsigned>(slots)), dim3(256), 0, s, true,
+                          static_cast<const int32_t*>(w.r.n_active), static_cast<const int32_t*>(w.r.act_expert),
+                          q.loc, q.n_dev_slots, q.n_host, static_cast<const uint8_t*>(q.hg),
+                          static_cast<const uint8_t*>(q.hu), static_cast<const uint8_t*>(q.hd), w.stage[0],
+                          w.stage[1], w.stage[2], gu, dn, w.src_sel, w.src_z);
+        if (e != cudaSuccess) return e;
+    }
+    if (token) {
+        MoeTokWs tw{};
+        tw.h = w.h;
+        tw.yp = w.yp;
+        tw.idx = w.r.idx;
+        tw.p = w.r.p;
+        tw.src_sel = w.src_sel;
+        tw.src_z = w.src_z;
+        for (int i = 0; i < 3; ++i) tw.stage[i] = w.stage[i];
+        tw.hx = w.tok_hx;
+        tw.epoch = w.tok_epoch;
+        tw.trace_id = tb + 1;
+        return moe_token_run(q, tw, s);
     }
     // row-resident grouped passes (3-D TMA unit stages)
     {
@@ -714,17 +703,6 @@ cudaError_t moe_run(const MoeReq& q, cudaStream_t s) {
                 !encode_expert_map(&su, q.qt, w.stage[1], slots, q.d_ff, q.d_model, 64) ||
                 !encode_expert_map(&sd, q.qt, w.stage[2], slots, q.d_model, q.d_ff, kMrRows))
                 return cudaErrorInvalidValue;
-            const int ub = q.qt == 0 ? Fmt<0>::unit_bytes : Fmt<1>::unit_bytes;
-            const int64_t gu = q.d_ff * (q.d_model / kUnitWeights) * ub;
-            const int64_t dn = q.d_model * (q.d_ff / kUnitWeights) * ub;
-            // enough CTAs per active expert to keep many host reads in flight
-            e = launch_kernel(moe_fetch_kernel, dim3(kFetchCtas, static_cast<unsigned>(slots)), dim3(256), 0, s, true,
-                              static_cast<const int32_t*>(w.r.n_active), static_cast<const int32_t*>(w.r.act_expert),
-                              q.loc, q.n_dev_slots, q.n_host, static_cast<const uint8_t*>(q.hg),
-                              static_cast<const uint8_t*>(q.hu),
-                              static_cast<const uint8_t*>(q.hd), w.stage[0], w.stage[1], w.stage[2], gu, dn,
-                              w.src_sel, w.src_z);
-            if (e != cudaSuccess) return e;
         }
         MoeRowsParams pg{};
         const size_t smem_g = moe_rows_layout(q.qt, q.d_model, &pg);

@@ -143,6 +143,23 @@ struct MoeReq {
 };
 size_t moe_ws_bytes(const MoeReq& q);
 cudaError_t moe_run(const MoeReq& q, cudaStream_t s);
+// One-token MoE in one cooperative kernel (moe_token.cu): the workspace
+// parts it uses, carved by moe_run.
+constexpr int kTokReplicas = 8;  // tagged copies of h (CTA i reads copy i % 8)
+struct MoeTokWs {
+    float* h;
+    float* yp;
+    int32_t* idx;
+    float* p;
+    int32_t* src_sel;
+    int32_t* src_z;
+    uint8_t* stage[3];
+    uint2* hx;        // {value, tag} copies of h: [kTokReplicas][top_k * d_ff]
+    unsigned* epoch;  // calls so far (zero in a fresh workspace)
+    int trace_id;
+};
+bool moe_token_fits(const MoeReq& q);
+cudaError_t moe_token_run(const MoeReq& q, const MoeTokWs& w, cudaStream_t s);
 
 // ---------------------------------------------------------------- prefill
 struct PrefillReq {
@@ -166,6 +183,7 @@ cudaError_t read_dev_err_decode_persistent(int* code);
 cudaError_t read_dev_err_gemv_rows(int* code);
 cudaError_t read_dev_err_attention(int* code);
 cudaError_t read_dev_err_gemv_xr(int* code);
+cudaError_t read_dev_err_moe_token(int* code);
 
 // Row-resident batched GEMV (gemv_rows.cu): plain store, batch 2..8,
 // K % 256 == 0. ksplit_out receives the K splits (> 1: partials in q.ws
