@@ -240,7 +240,8 @@ template <int QT>
 struct MrCfg {
     static constexpr int ub = Fmt<QT>::unit_bytes;
     static constexpr int stage_bytes = kMrRows * ub;
-    static constexpr int ns = QT == 0 ? 3 : 6;
+    static constexpr int ns = 3;
+    static constexpr int ctas_per_sm = QT == 0 ? 1 : 2;  // Q4_K: two CTAs per SM overlap one's staging with the other's dots
 };
 
 struct MoeRowsParams {
@@ -349,7 +350,7 @@ __device__ __forceinline__ bool moe_rows_group(const MoeRowsParams& p, const int
 }
 
 template <int QT, int NMAT>
-__global__ void __launch_bounds__(kMrThreads, 1)
+__global__ void __launch_bounds__(kMrThreads, MrCfg<QT>::ctas_per_sm)
     moe_rows_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
                     const __grid_constant__ CUtensorMap tm0b, const __grid_constant__ CUtensorMap tm1b,
                     const __grid_constant__ MoeRowsParams p) {

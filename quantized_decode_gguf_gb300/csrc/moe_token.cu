@@ -268,13 +268,19 @@ __global__ void __launch_bounds__(kTokThreads, 1) moe_token_kernel(const __grid_
     const int mat = rem / sh_in, pos = rem - mat * sh_in;
     const bool act = jp < p.pp;
     float* part = reinterpret_cast<float*>(smem + p.part_off);
+    auto publish = [&](int q, float hv, int r0, int nl) {  // lanes r0, r0 + nl, ... store the replicas
+        for (int rep = r0; rep < kRep; rep += nl) st_pair(p.hx + static_cast<int64_t>(rep) * G + g0 + q, hv, tag);
+        if (r0 == 0) p.h[g0 + q] = hv;
+    };
     {
         float xr[128];  // this phase's activations (a second array serves the down phase)
         float xf = 1.f;
         if (act) xf = load_xr_scaled(xs + pos * (kXPadEvery + kXPad), xr);
         for (int c = 0; c < nchunks; ++c) {
+            if (tid == 0 && c == nchunks - 1) PHB_TRACE_EV(p.trace_id, 15);
             if (!mbar_wait_warp(&full[c], 0, &g_dev_err)) break;
             if (tid == 0 && c == 0) PHB_TRACE_EV(p.trace_id, 7);
+            if (tid == 0 && c == nchunks - 1) PHB_TRACE_EV(p.trace_id, 14);
             const int q = c * p.pp + jp;
             if (act && q < rows_g) {
                 const uint8_t* unit = smem + p.wgu_off + (static_cast<size_t>(c) * p.pp * 2 + mat * p.pp + jp) * p.rb_in +
@@ -284,11 +290,11 @@ __global__ void __launch_bounds__(kTokThreads, 1) moe_token_kernel(const __grid_
         }
     }
     if (tid == 0) PHB_TRACE_EV(p.trace_id, 8);
-    consumer_sync<kTokNC>();
-    // eight lanes per row pair, four row pairs per warp: lanes 0-3 of a
-    // group add the gate row's half-unit sums, lanes 4-7 the up row's
-    // (strided, then a fixed xor tree); lane k of the group stores replica k
+    consumer_sync<kTokNC>();  // every dot is done: the gate/up weights' shared memory is free
     {
+        // eight lanes per row pair, four row pairs per warp: lanes 0-3 of a
+        // group add the gate row's half-unit sums, lanes 4-7 the up row's
+        // (strided, then a fixed xor tree); lane k of the group stores replica k
         const int grp = lane >> 3, gl = lane & 7;
         for (int q0 = 4 * warp; q0 < rows_g; q0 += 4 * kTokCW) {
             const int q = q0 + grp;
@@ -300,11 +306,7 @@ __global__ void __launch_bounds__(kTokThreads, 1) moe_token_kernel(const __grid_
             v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
             v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
             const float gate = __shfl_sync(0xFFFFFFFFu, v, lane & ~7), up = __shfl_sync(0xFFFFFFFFu, v, (lane & ~7) | 4);
-            if (q < rows_g) {
-                const float hv = silu_mul(gate, up);
-                st_pair(p.hx + static_cast<int64_t>(gl) * G + g0 + q, hv, tag);
-                if (gl == 0) p.h[g0 + q] = hv;
-            }
+            if (q < rows_g) publish(q, silu_mul(gate, up), gl, 8);
         }
     }
     if (tid == 0) PHB_TRACE_EV(p.trace_id, 2);
@@ -360,25 +362,27 @@ __global__ void __launch_bounds__(kTokThreads, 1) moe_token_kernel(const __grid_
     if (okd && act2) {
         float xr[128];
         const float xf = load_xr_scaled(hs + (r * sh_ff + hh) * (kXPadEvery + kXPad), xr);
+        if (tid == 0) PHB_TRACE_EV(p.trace_id, 10);
         for (int nl = jr; nl < rows_d; nl += rpass) {
             const uint8_t* unit = smem + p.wd_off + (static_cast<size_t>(r) * p.rd + nl) * p.rb_ff + (hh >> 1) * kUB;
             part[(nl * p.K + r) * sh_ff + hh] = half_dot<QT>(unit, hh & 1, xr, xf);
         }
+        if (tid == 0) PHB_TRACE_EV(p.trace_id, 11);
     }
     consumer_sync<kTokNC>();
-    float* ysm = part + p.rd * p.K * sh_ff;
-    for (int i = tid; i < rows_d * p.K; i += kTokNC) {
-        const int nl = i / p.K, rr = i - nl * p.K;
+    if (tid == 0) PHB_TRACE_EV(p.trace_id, 12);
+    // one warp per output row: lane r adds slot r's half-unit sums in order
+    // (y_pair), then the slots are combined in ascending order
+    for (int nl = warp; nl < rows_d; nl += kTokCW) {
         float v = 0.f;
-        for (int j = 0; j < sh_ff; ++j) v += part[i * sh_ff + j];
-        ysm[i] = v;
-        p.yp[static_cast<int64_t>(rr) * p.d_model + n0 + nl] = v;
-    }
-    consumer_sync<kTokNC>();
-    for (int nl = tid; nl < rows_d; nl += kTokNC) {
+        if (lane < p.K) {
+            const float* pr = part + (nl * p.K + lane) * sh_ff;
+            for (int j = 0; j < sh_ff; ++j) v += pr[j];
+            p.yp[static_cast<int64_t>(lane) * p.d_model + n0 + nl] = v;
+        }
         float acc = 0.f;
-        for (int rr = 0; rr < p.K; ++rr) acc = fmaf(sp[rr], ysm[nl * p.K + rr], acc);
-        p.y[n0 + nl] = acc;
+        for (int rr = 0; rr < p.K; ++rr) acc = fmaf(sp[rr], __shfl_sync(0xFFFFFFFFu, v, rr), acc);
+        if (lane == 0) p.y[n0 + nl] = acc;
     }
     // CTA 0 has read every CTA's h, so every CTA has read the epoch: advance it
     if (blockIdx.x == 0 && tid == 0) *p.epoch = tag;
