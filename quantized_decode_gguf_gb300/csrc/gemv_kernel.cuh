@@ -38,7 +38,7 @@ static __device__ int g_dev_err;
 
 #ifdef PHB_TRACE
 // Debug builds only: per-CTA timestamps [launch id][cta][event].
-constexpr int kTraceLaunches = 128, kTraceCtas = 160, kTraceEvents = 10;
+constexpr int kTraceLaunches = 128, kTraceCtas = 160, kTraceEvents = 16;
 static __device__ uint64_t g_trace[kTraceLaunches * kTraceCtas * kTraceEvents];
 #define PHB_TRACE_EV(id, ev)                                                                          \
     do {                                                                                              \
