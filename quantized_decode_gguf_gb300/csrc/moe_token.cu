@@ -352,11 +352,14 @@ __global__ void __launch_bounds__(kTokThreads, 1) moe_token_kernel(const __grid_
 
     // ---- down + combine
     const int sh_ff = 2 * (p.d_ff / kUnitWeights);
+    // position (slot r, half unit hh) = tid / rpass, row group jr = tid % rpass:
+    // the rpass threads that hold the same activations sit side by side, so
+    // a warp's register fill reads few distinct addresses (broadcasts)
     const int p2 = p.K * sh_ff;  // (slot, half unit) positions of a down row
-    const int jr = tid / p2, rem2 = tid - jr * p2;
-    const int r = rem2 / sh_ff, hh = rem2 - r * sh_ff;
     const int rpass = kTokNC / p2;
-    const bool act2 = jr < rpass;
+    const int pos2 = tid / rpass, jr = tid - pos2 * rpass;
+    const int r = pos2 / sh_ff, hh = pos2 - r * sh_ff;
+    const bool act2 = pos2 < p2;
     const bool okd = mbar_wait_warp(full_d, 0, &g_dev_err);
     if (tid == 0) PHB_TRACE_EV(p.trace_id, 9);
     if (okd && act2) {
