@@ -133,71 +133,73 @@ __device__ __forceinline__ void st_chunk(uint8_t* tile, int row, int ch, uint32_
     *dst = make_uint4(a, b, c, d);
 }
 
-// Exact small-integer conversion: 0x4B0000bb is the float 2^23 + bb.
+// Byte SEL of w as the float 2^23 + byte (exact).
 template <int SEL>
-__device__ __forceinline__ float byte_int(uint32_t w, float bias) {
-    return __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7440u | SEL)) - bias;
+__device__ __forceinline__ float byte_magic(uint32_t w) {
+    return __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7440u | SEL));
+}
+
+__device__ __forceinline__ float byte_magic_rt(uint32_t w, int sel) {
+    return __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7440u | static_cast<uint32_t>(sel)));
 }
 
 // One K block (64 weights) of a Q8_0 unit held in registers (68 words).
+// Two weights per packed operation: (2^23 + u) - (2^23 + 128) = q and d q,
+// both exact, then one rounding to bf16.
 template <int J>
 __device__ __forceinline__ void dequant_q8_0_kb(const uint32_t (&u)[68], uint8_t* tile, int row) {
+    const float2 bias = make_float2(-8388736.0f, -8388736.0f);
 #pragma unroll
     for (int hb = 0; hb < 2; ++hb) {
         const int ob = 68 * J + 34 * hb;  // byte offset of the block in the unit
         const uint32_t dw = u[ob / 4];
         const float d = fp16_bits_to_float((ob % 4) ? (dw >> 16) : dw);
-        float w[32];
+        const float2 d2 = make_float2(d, d);
+        uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int p = ob + 2 + i;
-            const uint32_t word = u[p / 4] ^ 0x80808080u;
-            float q;
-            switch (p % 4) {
-                case 0: q = byte_int<0>(word, 8388736.0f); break;
-                case 1: q = byte_int<1>(word, 8388736.0f); break;
-                case 2: q = byte_int<2>(word, 8388736.0f); break;
-                default: q = byte_int<3>(word, 8388736.0f); break;
-            }
-            w[i] = d * q;  // exact
+        for (int i = 0; i < 32; i += 2) {
+            const int p0 = ob + 2 + i, p1 = p0 + 1;
+            const float2 m = make_float2(byte_magic_rt(u[p0 / 4] ^ 0x80808080u, p0 % 4),
+                                         byte_magic_rt(u[p1 / 4] ^ 0x80808080u, p1 % 4));
+            const float2 w = __fmul2_rn(d2, __fadd2_rn(m, bias));  // exact
+            pk[i / 2] = pack_bf16(w.x, w.y);
         }
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-            st_chunk(tile, row, 4 * hb + c, pack_bf16(w[8 * c], w[8 * c + 1]), pack_bf16(w[8 * c + 2], w[8 * c + 3]),
-                     pack_bf16(w[8 * c + 4], w[8 * c + 5]), pack_bf16(w[8 * c + 6], w[8 * c + 7]));
+        for (int c = 0; c < 4; ++c) st_chunk(tile, row, 4 * hb + c, pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
     }
 }
 
-// One K block (64 weights: sub-blocks 2J and 2J+1) of a Q4_K block in registers (36 words).
+// One K block (64 weights: sub-blocks 2J and 2J+1) of a Q4_K block in
+// registers (36 words). Two weights per packed operation: the nibble as
+// (2^23 + q) - 2^23 = q exactly, then one rounding of D q - M (fma), then bf16.
 template <int J>
 __device__ __forceinline__ void dequant_q4_k_kb(const uint32_t (&u)[36], uint8_t* tile, int row) {
     const float d = fp16_bits_to_float(u[0]);
     const float dmin = fp16_bits_to_float(u[0] >> 16);
     const uint32_t sw[3] = {u[1], u[2], u[3]};
+    const float2 magic = make_float2(-8388608.0f, -8388608.0f);
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
         uint32_t sc, m;
         q4_k_scale_min(sw, 2 * J + half, sc, m);
         const float D = d * static_cast<float>(sc);     // exact
         const float M = dmin * static_cast<float>(m);   // exact
-        float w[32];
+        const float2 D2 = make_float2(D, D), nM2 = make_float2(-M, -M);
+        uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const uint32_t word = u[4 + 8 * J + i / 4];
+        for (int i4 = 0; i4 < 8; ++i4) {
+            const uint32_t word = u[4 + 8 * J + i4];
             const uint32_t nib = (half ? (word >> 4) : word) & 0x0F0F0F0Fu;
-            float q;
-            switch (i % 4) {
-                case 0: q = byte_int<0>(nib, 8388608.0f); break;
-                case 1: q = byte_int<1>(nib, 8388608.0f); break;
-                case 2: q = byte_int<2>(nib, 8388608.0f); break;
-                default: q = byte_int<3>(nib, 8388608.0f); break;
-            }
-            w[i] = fmaf(D, q, -M);  // one rounding of the exact D*q - M
+            const float2 q01 = __fadd2_rn(make_float2(byte_magic<0>(nib), byte_magic<1>(nib)), magic);
+            const float2 q23 = __fadd2_rn(make_float2(byte_magic<2>(nib), byte_magic<3>(nib)), magic);
+            const float2 w01 = __ffma2_rn(D2, q01, nM2);  // one rounding of the exact D q - M
+            const float2 w23 = __ffma2_rn(D2, q23, nM2);
+            pk[2 * i4] = pack_bf16(w01.x, w01.y);
+            pk[2 * i4 + 1] = pack_bf16(w23.x, w23.y);
         }
 #pragma unroll
         for (int c = 0; c < 4; ++c)
-            st_chunk(tile, row, 4 * half + c, pack_bf16(w[8 * c], w[8 * c + 1]), pack_bf16(w[8 * c + 2], w[8 * c + 3]),
-                     pack_bf16(w[8 * c + 4], w[8 * c + 5]), pack_bf16(w[8 * c + 6], w[8 * c + 7]));
+            st_chunk(tile, row, 4 * half + c, pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
     }
 }
 
