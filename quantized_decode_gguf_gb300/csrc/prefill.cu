@@ -47,16 +47,28 @@ namespace {
 constexpr int kBM = 128;                   // weight rows per CTA (MMA M)
 constexpr int kBN = 256;                   // tokens per CTA (MMA N)
 constexpr int kBK = 64;                    // K per stage: one 128-byte bf16 row
-constexpr int kStages = 4;
 constexpr int kATile = kBM * kBK * 2;      // 16 KB
 constexpr int kBTile = kBN * kBK * 2;      // 32 KB
-constexpr int kThreads = 256;
 constexpr int kProducerWarps = 4;          // warps 0-3: dequant producers, then epilogue
-constexpr int kTmaWarp = 4;
+constexpr int kTmaWarp = 4;                // token tiles
 constexpr int kMmaWarp = 5;
+constexpr int kRawWarp = 6;                // raw weight units
+constexpr int kThreads = 32 * (kRawWarp + 1);
+// Per format: Q8_0 stages its raw 256-weight units (128 rows x 272 bytes) in
+// shared memory by TMA, which leaves room for three bf16 stages; Q4_K keeps
+// four stages and double-buffers its raw units (144 bytes a row) in
+// registers, read by each producer thread from global memory.
+template <int QT>
+struct PCfg {
+    static constexpr bool staged = QT == 0;
+    static constexpr int stages = staged ? 3 : 4;
+    static constexpr int raw_stages = staged ? 2 : 0;
+    static constexpr int raw_bytes = kBM * 272;  // one raw slot
+    static constexpr size_t smem =
+        stages * (kATile + kBTile) + raw_stages * raw_bytes + 1024 /* align */ + 256 /* barriers */;
+};
 constexpr uint32_t kTmemCols = 256;
 constexpr int kKbPerUnit = 4;              // a 256-weight unit spans four K blocks
-constexpr size_t kSmemBytes = kStages * (kATile + kBTile) + 1024 /* align */ + 256 /* barriers */;
 
 struct PrefillParams {
     const uint8_t* w;
@@ -218,15 +230,24 @@ __device__ __forceinline__ void load_unit(const uint8_t* src, uint32_t (&u)[NW])
 // ---------------------------------------------------------------- the GEMM kernel
 template <int QT>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ PrefillParams p) {
+    prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
+                        const __grid_constant__ PrefillParams p) {
+    constexpr int kStages = PCfg<QT>::stages;
+    constexpr int kRawStages = PCfg<QT>::raw_stages > 0 ? PCfg<QT>::raw_stages : 1;
+    constexpr int kRawBytesMax = PCfg<QT>::raw_stages * PCfg<QT>::raw_bytes;
+    constexpr int UB = QT == 0 ? 272 : 144;      // bytes of one 256-weight unit of a row
+    constexpr int kUnitElems = QT == 0 ? 136 : 144;  // the same in tensor-map elements (u16 / u8)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t{1023});
     uint8_t* sA = smem;
     uint8_t* sB = smem + kStages * kATile;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStages * kBTile);
+    uint8_t* sR = sB + kStages * kBTile;  // staged raw units: [raw stages][128 rows][UB]
+    uint64_t* full = reinterpret_cast<uint64_t*>(sR + kRawBytesMax);
     uint64_t* empty = full + kStages;
     uint64_t* accb = empty + kStages;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
+    uint64_t* rfull = accb + 1;
+    uint64_t* rempty = rfull + kRawStages;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rempty + kRawStages);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -243,6 +264,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&empty[s], 1);
         }
         mbar_init(accb, 1);
+        for (int s = 0; s < PCfg<QT>::raw_stages; ++s) {
+            mbar_init(&rfull[s], 1);
+            mbar_init(&rempty[s], kProducerWarps);
+        }
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -261,13 +286,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp < kProducerWarps) {
         // ---------------- dequant producers: thread tid owns weight row n0 + tid
         const int row = tid;
-        const uint8_t* wr = p.w + (n0 + row) * p.row_bytes;
-        constexpr int UB = QT == 0 ? 272 : 144;
         constexpr int NW = UB / 4;
-        uint32_t cur[NW], nxt[NW];
-        if (nu > 0) load_unit<NW>(wr + static_cast<int64_t>(u0) * UB, cur);
+        uint32_t cur[NW];
+        [[maybe_unused]] uint32_t nxt[PCfg<QT>::staged ? 1 : NW];
+        const uint8_t* wr = p.w + (n0 + row) * p.row_bytes;
+        if constexpr (!PCfg<QT>::staged)
+            if (nu > 0) load_unit<NW>(wr + static_cast<int64_t>(u0) * UB, cur);
         for (int uu = 0; uu < nu; ++uu) {
-            if (uu + 1 < nu) load_unit<NW>(wr + static_cast<int64_t>(u0 + uu + 1) * UB, nxt);
+            if constexpr (PCfg<QT>::staged) {
+                // this row's raw unit from the staged copy of the CTA's 128 rows
+                const int rs = uu % kRawStages;
+                if (!mbar_wait_warp(&rfull[rs], (uu / kRawStages) & 1, &g_dev_err_prefill)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                const uint8_t* src = sR + rs * PCfg<QT>::raw_bytes + row * UB;
+#pragma unroll
+                for (int i = 0; i < NW / 4; ++i) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(src + 16 * i);
+                    cur[4 * i] = v.x;
+                    cur[4 * i + 1] = v.y;
+                    cur[4 * i + 2] = v.z;
+                    cur[4 * i + 3] = v.w;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&rempty[rs]);  // the slot may be refilled
+            } else {
+                if (uu + 1 < nu) load_unit<NW>(wr + static_cast<int64_t>(u0 + uu + 1) * UB, nxt);
+            }
 #pragma unroll
             for (int j = 0; j < kKbPerUnit; ++j) {
                 const int i = uu * kKbPerUnit + j;
@@ -293,8 +339,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive(&full[s]);
             }
             if (*abort_flag) break;
+            if constexpr (!PCfg<QT>::staged) {
 #pragma unroll
-            for (int i = 0; i < NW; ++i) cur[i] = nxt[i];
+                for (int i = 0; i < NW; ++i) cur[i] = nxt[i];
+            }
         }
     } else if (warp == kTmaWarp) {
         // ---------------- token tiles by TMA
@@ -314,6 +362,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             // normal path these phases completed long ago.
             for (int i = max(0, nkb - kStages); i < nkb; ++i)
                 mbar_wait(&full[i % kStages], (i / kStages) & 1, &g_dev_err_prefill);
+        }
+    } else if (PCfg<QT>::staged && warp == kRawWarp) {
+        // ---------------- raw weight units by TMA (weights never depend on the previous kernel)
+        if (lane == 0) {
+            for (int uu = 0; uu < nu; ++uu) {
+                const int rs = uu % kRawStages;
+                if (uu >= kRawStages && !mbar_wait(&rempty[rs], ((uu / kRawStages) - 1) & 1, &g_dev_err_prefill)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                mbar_arrive_expect_tx(&rfull[rs], static_cast<uint32_t>(kBM * UB));
+                tma_load_2d(sR + rs * PCfg<QT>::raw_bytes, &tmap_w, (u0 + uu) * kUnitElems, static_cast<int>(n0), &rfull[rs]);
+            }
+            // every copy into shared memory must land before the CTA exits (bounded waits)
+            for (int uu = max(0, nu - kRawStages); uu < nu; ++uu)
+                mbar_wait(&rfull[uu % kRawStages], (uu / kRawStages) & 1, &g_dev_err_prefill);
         }
     } else if (warp == kMmaWarp) {
         // ---------------- one thread issues the MMAs
@@ -461,6 +525,21 @@ cudaError_t prefill_run(const PrefillReq& q, cudaStream_t s) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
 
+    // weights [n][row bytes] as a 2-D tensor: one box = one 256-weight unit of 128 rows
+    // (u16 elements for Q8_0 so the 272-byte unit stays within the 256-element box limit)
+    CUtensorMap tmap_w;
+    {
+        const int64_t row_bytes = q.qt == 0 ? q.k / 32 * 34 : q.k / 256 * 144;
+        const int esz = q.qt == 0 ? 2 : 1;
+        const cuuint64_t wd[2] = {static_cast<cuuint64_t>(row_bytes / esz), static_cast<cuuint64_t>(q.n)};
+        const cuuint64_t ws_[1] = {static_cast<cuuint64_t>(row_bytes)};
+        const cuuint32_t wb[2] = {static_cast<cuuint32_t>((q.qt == 0 ? 272 : 144) / esz), static_cast<cuuint32_t>(kBM)};
+        if (encode(&tmap_w, q.qt == 0 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                   const_cast<void*>(q.w), wd, ws_, wb, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+
     const int64_t count8 = q.m * q.k / 8;
     cudaError_t e = launch_kernel(cast_bf16_kernel, dim3(static_cast<unsigned>(std::min<int64_t>(
                                                           (count8 + 255) / 256, int64_t{device_sm_count()} * 8))),
@@ -482,11 +561,11 @@ cudaError_t prefill_run(const PrefillReq& q, cudaStream_t s) {
     if (q.qt == 0) {
         constexpr auto kern = prefill_gemm_kernel<0>;
         if ((e = ensure_smem_attr<kern>()) != cudaSuccess) return e;
-        e = launch_kernel(kern, grid, dim3(kThreads), kSmemBytes, s, true, tmap, p);
+        e = launch_kernel(kern, grid, dim3(kThreads), PCfg<0>::smem, s, true, tmap, tmap_w, p);
     } else {
         constexpr auto kern = prefill_gemm_kernel<1>;
         if ((e = ensure_smem_attr<kern>()) != cudaSuccess) return e;
-        e = launch_kernel(kern, grid, dim3(kThreads), kSmemBytes, s, true, tmap, p);
+        e = launch_kernel(kern, grid, dim3(kThreads), PCfg<1>::smem, s, true, tmap, tmap_w, p);
     }
     if (e != cudaSuccess || sp.splits == 1) return e;
     const int64_t count4 = q.m * q.n / 4;
