@@ -3,18 +3,23 @@
 //   Y[t][n] = sum_k bf16(w[n][k]) * bf16(X[t][k]),  fp32 accumulation.
 //
 // The weights are the MMA's M operand: a CTA owns 128 weight rows and 256
-// tokens (D = 128 x 256 fp32 in TMEM, 256 columns). Per 64-wide K block:
-//  - four producer warps dequantise their rows (one row per thread, raw
-//    blocks double-buffered in registers from global memory) to bf16 and
-//    store them in the 128-byte-swizzled K-major layout the MMA reads;
+// tokens (D = 128 x 256 fp32 in TMEM, columns 0-255). Per 64-wide K block:
+//  - four producer warps dequantise their rows (one row per thread) to bf16
+//    and write them straight into TMEM with tcgen05.st (lane = weight row,
+//    32 columns of bf16 pairs per K block, one slot per stage after the
+//    accumulator): the MMA reads its A operand from TMEM, so the weight tile
+//    never passes through shared memory and needs no proxy fence. Raw units
+//    come from global memory into a register double buffer (Q4_K) or are
+//    staged in shared memory by a 2-D TMA copy per 256-weight unit of the
+//    CTA's 128 rows (Q8_0);
 //  - one thread loads the token tile (bf16, 256 x 64) with a 2-D TMA copy
-//    into the same swizzled layout;
-//  - one thread issues four tcgen05.mma (M128 N256 K16) and commits them to
-//    the stage's "empty" barrier;
-// after the last K block the four producer warps drain TMEM (tcgen05.ld,
-// one TMEM lane per weight row) and write Y, or a split-K partial that a
-// second kernel reduces in split order. X is cast to bf16 (round to nearest
-// even) by a first kernel into the caller's workspace.
+//    into the 128-byte-swizzled K-major layout the MMA reads;
+//  - one thread issues four tcgen05.mma (M128 N256 K16, A in TMEM, B in
+//    shared memory) and commits them to the stage's "empty" barrier;
+// after the last K block the four producer warps drain the accumulator
+// (tcgen05.ld, one TMEM lane per weight row) and write Y, or a split-K
+// partial that a second kernel reduces in split order. X is cast to bf16
+// (round to nearest even) by a first kernel into the caller's workspace.
 //
 // Every wait is bounded; a wait that runs out sets this translation unit's
 // device error word, the kernel drains and frees its TMEM and returns.
@@ -47,7 +52,6 @@ namespace {
 constexpr int kBM = 128;                   // weight rows per CTA (MMA M)
 constexpr int kBN = 256;                   // tokens per CTA (MMA N)
 constexpr int kBK = 64;                    // K per stage: one 128-byte bf16 row
-constexpr int kATile = kBM * kBK * 2;      // 16 KB
 constexpr int kBTile = kBN * kBK * 2;      // 32 KB
 constexpr int kProducerWarps = 4;          // warps 0-3: dequant producers, then epilogue
 constexpr int kTmaWarp = 4;                // token tiles
@@ -65,9 +69,13 @@ struct PCfg {
     static constexpr int raw_stages = staged ? 2 : 0;
     static constexpr int raw_bytes = kBM * 272;  // one raw slot
     static constexpr size_t smem =
-        stages * (kATile + kBTile) + raw_stages * raw_bytes + 1024 /* align */ + 256 /* barriers */;
+        stages * kBTile + raw_stages * raw_bytes + 1024 /* align */ + 256 /* barriers */;
 };
-constexpr uint32_t kTmemCols = 256;
+// TMEM: the fp32 accumulator in columns 0-255, then one 32-column slot per
+// stage for the bf16 weight tile (the MMA's A operand, read from TMEM: lane
+// = weight row, column c = the bf16 pair k = 2c, 2c + 1 of the K block).
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAcol0 = 256;
 constexpr int kKbPerUnit = 4;              // a 256-weight unit spans four K blocks
 
 struct PrefillParams {
@@ -97,6 +105,16 @@ __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64
         "setp.ne.u32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
         "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+        : "memory");
+}
+
+// The same with A read from TMEM (128 lanes x 8 columns of bf16 pairs per K = 16).
+__device__ __forceinline__ void mma_bf16_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
         : "memory");
 }
 
@@ -132,17 +150,24 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// ---------------------------------------------------------------- dequant to swizzled bf16
+// 32 consecutive TMEM columns of this warp's 32 lanes from 32 registers a thread, then
+// wait until the stores are done.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+        "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+        "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- dequant to bf16 pairs
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     const __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<const uint32_t*>(&t);
-}
-
-// Store 16-byte chunk `ch` (8 bf16, k = 8ch..8ch+7) of tile row `row`.
-__device__ __forceinline__ void st_chunk(uint8_t* tile, int row, int ch, uint32_t a, uint32_t b, uint32_t c,
-                                         uint32_t d) {
-    uint4* dst = reinterpret_cast<uint4*>(tile + row * 128 + ((ch ^ (row & 7)) << 4));
-    *dst = make_uint4(a, b, c, d);
 }
 
 // Byte SEL of w as the float 2^23 + byte (exact).
@@ -159,7 +184,7 @@ __device__ __forceinline__ float byte_magic_rt(uint32_t w, int sel) {
 // Two weights per packed operation: (2^23 + u) - (2^23 + 128) = q and d q,
 // both exact, then one rounding to bf16.
 template <int J>
-__device__ __forceinline__ void dequant_q8_0_kb(const uint32_t (&u)[68], uint8_t* tile, int row) {
+__device__ __forceinline__ void dequant_q8_0_kb(const uint32_t (&u)[68], uint32_t (&out)[32]) {
     const float2 bias = make_float2(-8388736.0f, -8388736.0f);
 #pragma unroll
     for (int hb = 0; hb < 2; ++hb) {
@@ -167,17 +192,14 @@ __device__ __forceinline__ void dequant_q8_0_kb(const uint32_t (&u)[68], uint8_t
         const uint32_t dw = u[ob / 4];
         const float d = fp16_bits_to_float((ob % 4) ? (dw >> 16) : dw);
         const float2 d2 = make_float2(d, d);
-        uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
             const int p0 = ob + 2 + i, p1 = p0 + 1;
             const float2 m = make_float2(byte_magic_rt(u[p0 / 4] ^ 0x80808080u, p0 % 4),
                                          byte_magic_rt(u[p1 / 4] ^ 0x80808080u, p1 % 4));
             const float2 w = __fmul2_rn(d2, __fadd2_rn(m, bias));  // exact
-            pk[i / 2] = pack_bf16(w.x, w.y);
+            out[16 * hb + i / 2] = pack_bf16(w.x, w.y);
         }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) st_chunk(tile, row, 4 * hb + c, pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
     }
 }
 
@@ -185,7 +207,7 @@ __device__ __forceinline__ void dequant_q8_0_kb(const uint32_t (&u)[68], uint8_t
 // registers (36 words). Two weights per packed operation: the nibble as
 // (2^23 + q) - 2^23 = q exactly, then one rounding of D q - M (fma), then bf16.
 template <int J>
-__device__ __forceinline__ void dequant_q4_k_kb(const uint32_t (&u)[36], uint8_t* tile, int row) {
+__device__ __forceinline__ void dequant_q4_k_kb(const uint32_t (&u)[36], uint32_t (&out)[32]) {
     const float d = fp16_bits_to_float(u[0]);
     const float dmin = fp16_bits_to_float(u[0] >> 16);
     const uint32_t sw[3] = {u[1], u[2], u[3]};
@@ -197,7 +219,6 @@ __device__ __forceinline__ void dequant_q4_k_kb(const uint32_t (&u)[36], uint8_t
         const float D = d * static_cast<float>(sc);     // exact
         const float M = dmin * static_cast<float>(m);   // exact
         const float2 D2 = make_float2(D, D), nM2 = make_float2(-M, -M);
-        uint32_t pk[16];
 #pragma unroll
         for (int i4 = 0; i4 < 8; ++i4) {
             const uint32_t word = u[4 + 8 * J + i4];
@@ -206,12 +227,9 @@ __device__ __forceinline__ void dequant_q4_k_kb(const uint32_t (&u)[36], uint8_t
             const float2 q23 = __fadd2_rn(make_float2(byte_magic<2>(nib), byte_magic<3>(nib)), magic);
             const float2 w01 = __ffma2_rn(D2, q01, nM2);  // one rounding of the exact D q - M
             const float2 w23 = __ffma2_rn(D2, q23, nM2);
-            pk[2 * i4] = pack_bf16(w01.x, w01.y);
-            pk[2 * i4 + 1] = pack_bf16(w23.x, w23.y);
+            out[16 * half + 2 * i4] = pack_bf16(w01.x, w01.y);
+            out[16 * half + 2 * i4 + 1] = pack_bf16(w23.x, w23.y);
         }
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-            st_chunk(tile, row, 4 * half + c, pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
     }
 }
 
@@ -239,8 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kUnitElems = QT == 0 ? 136 : 144;  // the same in tensor-map elements (u16 / u8)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t{1023});
-    uint8_t* sA = smem;
-    uint8_t* sB = smem + kStages * kATile;
+    uint8_t* sB = smem;
     uint8_t* sR = sB + kStages * kBTile;  // staged raw units: [raw stages][128 rows][UB]
     uint64_t* full = reinterpret_cast<uint64_t*>(sR + kRawBytesMax);
     uint64_t* empty = full + kStages;
@@ -322,19 +339,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *abort_flag = 1;
                     break;
                 }
-                uint8_t* tile = sA + s * kATile;
+                tc_fence_after();  // the MMAs that read this slot have completed (empty barrier)
+                uint32_t pk[32];
                 if constexpr (QT == 0) {
-                    if (j == 0) dequant_q8_0_kb<0>(cur, tile, row);
-                    else if (j == 1) dequant_q8_0_kb<1>(cur, tile, row);
-                    else if (j == 2) dequant_q8_0_kb<2>(cur, tile, row);
-                    else dequant_q8_0_kb<3>(cur, tile, row);
+                    if (j == 0) dequant_q8_0_kb<0>(cur, pk);
+                    else if (j == 1) dequant_q8_0_kb<1>(cur, pk);
+                    else if (j == 2) dequant_q8_0_kb<2>(cur, pk);
+                    else dequant_q8_0_kb<3>(cur, pk);
                 } else {
-                    if (j == 0) dequant_q4_k_kb<0>(cur, tile, row);
-                    else if (j == 1) dequant_q4_k_kb<1>(cur, tile, row);
-                    else if (j == 2) dequant_q4_k_kb<2>(cur, tile, row);
-                    else dequant_q4_k_kb<3>(cur, tile, row);
+                    if (j == 0) dequant_q4_k_kb<0>(cur, pk);
+                    else if (j == 1) dequant_q4_k_kb<1>(cur, pk);
+                    else if (j == 2) dequant_q4_k_kb<2>(cur, pk);
+                    else dequant_q4_k_kb<3>(cur, pk);
                 }
-                fence_proxy_async_smem();
+                tmem_st32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + kAcol0 + 32 * s, pk);
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&full[s]);
             }
@@ -392,9 +411,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < kBK / 16; ++kk) {
-                    const uint64_t ad = smem_desc_sw128(sA + s * kATile + kk * 32);
                     const uint64_t bd = smem_desc_sw128(sB + s * kBTile + kk * 32);
-                    mma_bf16(tmem, ad, bd, (i > 0 || kk > 0) ? 1u : 0u);
+                    mma_bf16_ta(tmem, tmem + kAcol0 + 32 * s + 8 * kk, bd, (i > 0 || kk > 0) ? 1u : 0u);
                 }
                 mma_commit(&empty[s]);
             }
