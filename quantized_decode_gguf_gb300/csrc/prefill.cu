@@ -58,24 +58,27 @@ constexpr int kTmaWarp = 4;                // token tiles
 constexpr int kMmaWarp = 5;
 constexpr int kRawWarp = 6;                // raw weight units
 constexpr int kThreads = 32 * (kRawWarp + 1);
-// Per format: Q8_0 stages its raw 256-weight units (128 rows x 272 bytes) in
-// shared memory by TMA, which leaves room for three bf16 stages; Q4_K keeps
-// four stages and double-buffers its raw units (144 bytes a row) in
-// registers, read by each producer thread from global memory.
-template <int QT>
-struct PCfg {
-    static constexpr bool staged = QT == 0;
-    static constexpr int stages = staged ? 3 : 4;
-    static constexpr int raw_stages = staged ? 2 : 0;
-    static constexpr int raw_bytes = kBM * 272;  // one raw slot
-    static constexpr size_t smem =
-        stages * kBTile + raw_stages * raw_bytes + 1024 /* align */ + 256 /* barriers */;
-};
 // TMEM: the fp32 accumulator in columns 0-255, then one 32-column slot per
 // stage for the bf16 weight tile (the MMA's A operand, read from TMEM: lane
 // = weight row, column c = the bf16 pair k = 2c, 2c + 1 of the K block).
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAcol0 = 256;
+
+// Per format: Q8_0 stages its raw 256-weight units (128 rows x 272 bytes) in
+// shared memory by TMA, beside four token-tile stages; Q4_K double-buffers
+// its raw units (144 bytes a row) in registers, read by each producer thread
+// from global memory, and keeps six stages. (TMEM holds the accumulator and
+// one 32-column weight slot per stage: at most 8 stages.)
+template <int QT>
+struct PCfg {
+    static constexpr bool staged = QT == 0;
+    static constexpr int stages = staged ? 4 : 6;
+    static constexpr int raw_stages = staged ? 2 : 0;
+    static constexpr int raw_bytes = kBM * 272;  // one raw slot
+    static_assert(kAcol0 + 32 * stages <= kTmemCols, "a weight slot per stage after the accumulator");
+    static constexpr size_t smem =
+        stages * kBTile + raw_stages * raw_bytes + 1024 /* align */ + 256 /* barriers */;
+};
 constexpr int kKbPerUnit = 4;              // a 256-weight unit spans four K blocks
 
 struct PrefillParams {
