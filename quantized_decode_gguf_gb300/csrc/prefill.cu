@@ -4,8 +4,9 @@
 //
 // The weights are the MMA's M operand: a CTA owns 128 weight rows and 256
 // tokens (D = 128 x 256 fp32 in TMEM, columns 0-255). Per 64-wide K block:
-//  - four producer warps dequantise their rows (one row per thread) to bf16
-//    and write them straight into TMEM with tcgen05.st (lane = weight row,
+//  - eight producer warps, in two groups taking alternate K blocks,
+//    dequantise their rows (one row per thread) to bf16 and write them
+//    straight into TMEM with tcgen05.st (lane = weight row,
 //    32 columns of bf16 pairs per K block, one slot per stage after the
 //    accumulator): the MMA reads its A operand from TMEM, so the weight tile
 //    never passes through shared memory and needs no proxy fence. Raw units
@@ -53,10 +54,11 @@ constexpr int kBM = 128;                   // weight rows per CTA (MMA M)
 constexpr int kBN = 256;                   // tokens per CTA (MMA N)
 constexpr int kBK = 64;                    // K per stage: one 128-byte bf16 row
 constexpr int kBTile = kBN * kBK * 2;      // 32 KB
-constexpr int kProducerWarps = 4;          // warps 0-3: dequant producers, then epilogue
-constexpr int kTmaWarp = 4;                // token tiles
-constexpr int kMmaWarp = 5;
-constexpr int kRawWarp = 6;                // raw weight units
+constexpr int kProducerWarps = 4;          // warps per K block, one weight row per thread; warps 0-3 drain TMEM
+constexpr int kProducerGroups = 2;         // groups of producer warps, taking alternate K blocks
+constexpr int kTmaWarp = kProducerWarps * kProducerGroups;  // token tiles
+constexpr int kMmaWarp = kTmaWarp + 1;
+constexpr int kRawWarp = kTmaWarp + 2;     // raw weight units
 constexpr int kThreads = 32 * (kRawWarp + 1);
 // TMEM: the fp32 accumulator in columns 0-255, then one 32-column slot per
 // stage for the bf16 weight tile (the MMA's A operand, read from TMEM: lane
@@ -286,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(accb, 1);
         for (int s = 0; s < PCfg<QT>::raw_stages; ++s) {
             mbar_init(&rfull[s], 1);
-            mbar_init(&rempty[s], kProducerWarps);
+            mbar_init(&rempty[s], kProducerWarps * kProducerGroups);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -303,9 +305,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     pdl_launch_dependents();
 
-    if (warp < kProducerWarps) {
-        // ---------------- dequant producers: thread tid owns weight row n0 + tid
-        const int row = tid;
+    if (warp < kProducerWarps * kProducerGroups) {
+        // ---------------- dequant producers: thread tid owns weight row n0 + tid % 128 and,
+        // in group g = tid / 128, the K blocks j = g, g + groups, ... of every unit
+        const int row = tid & (kBM - 1);
+        const int grp = tid / kBM;
         constexpr int NW = UB / 4;
         uint32_t cur[NW];
         [[maybe_unused]] uint32_t nxt[PCfg<QT>::staged ? 1 : NW];
@@ -336,6 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 #pragma unroll
             for (int j = 0; j < kKbPerUnit; ++j) {
+                if (j % kProducerGroups != grp) continue;
                 const int i = uu * kKbPerUnit + j;
                 const int s = i % kStages;
                 if (i >= kStages && !mbar_wait_warp(&empty[s], ((i / kStages) - 1) & 1, &g_dev_err_prefill)) {
@@ -355,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     else if (j == 2) dequant_q4_k_kb<2>(cur, pk);
                     else dequant_q4_k_kb<3>(cur, pk);
                 }
-                tmem_st32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + kAcol0 + 32 * s, pk);
+                tmem_st32(tmem + (static_cast<uint32_t>(32 * (warp % kProducerWarps)) << 16) + kAcol0 + 32 * s, pk);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&full[s]);
