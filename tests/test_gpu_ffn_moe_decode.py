@@ -105,6 +105,9 @@ MOE_CASES = [
     ("q4_k", 64, 32, 8, 256, 256),     # many tokens per expert (groups of 4)
     ("q8_0", 1, 16, 4, 512, 256),      # one token, other shapes
     ("q4_k", 1, 8, 2, 256, 512),
+    ("q4_k", 1, 64, 6, 1024, 512),     # one-token kernel: 22 row pairs per chunk, six slots
+    ("q8_0", 1, 40, 3, 768, 256),      # one-token kernel: odd unit count, three slots
+    ("q4_k", 1, 256, 8, 2048, 1024),   # one-token kernel: 256 experts, five chunks per CTA
 ]
 
 
