@@ -196,7 +196,6 @@ __global__ void __launch_bounds__(kTokThreads, 1) moe_token_kernel(const __grid_
             const int q0 = c * p.pp, q1 = min(rows_g, q0 + p.pp);
             route_to((g0 + q1 - 1) / p.d_ff);
             if (lane == 0) {
-                if (c == 0) PHB_TRACE_EV(p.trace_id, 5);
                 uint32_t tx = 0;
                 for (int q = q0; q < q1;) {
                     const int g = g0 + q, slot = g / p.d_ff, row = g - slot * p.d_ff;
@@ -244,7 +243,6 @@ __global__ void __launch_bounds__(kTokThreads, 1) moe_token_kernel(const __grid_
                         bulk_g2s_hint(smem + p.wd_off + static_cast<size_t>(r) * p.rd * p.rb_ff,
                                       base(r, p.wd, p.sd, dn_bytes) + static_cast<int64_t>(n0) * p.rb_ff,
                                       static_cast<uint32_t>(rows_d) * p.rb_ff, full_d, pol);
-            PHB_TRACE_EV(p.trace_id, 6);
             // stay until every copy into this CTA's shared memory has landed (bounded)
             for (int c = 0; c < nchunks; ++c) mbar_wait(&full[c], 0, &g_dev_err);
             mbar_wait(full_d, 0, &g_dev_err);
@@ -255,7 +253,6 @@ __global__ void __launch_bounds__(kTokThreads, 1) moe_token_kernel(const __grid_
     // ---- consumers: gate/up
     pdl_wait();  // x and the epoch come from earlier kernels
     const unsigned tag = __ldcg(p.epoch) + 1u;
-    if (tid == 0) PHB_TRACE_EV(p.trace_id, 1);
     float* xs = reinterpret_cast<float*>(smem + p.xs_off);
     {
         const float4* xg = reinterpret_cast<const float4*>(p.x);
@@ -277,10 +274,7 @@ __global__ void __launch_bounds__(kTokThreads, 1) moe_token_kernel(const __grid_
         float xf = 1.f;
         if (act) xf = load_xr_scaled(xs + pos * (kXPadEvery + kXPad), xr);
         for (int c = 0; c < nchunks; ++c) {
-            if (tid == 0 && c == nchunks - 1) PHB_TRACE_EV(p.trace_id, 15);
             if (!mbar_wait_warp(&full[c], 0, &g_dev_err)) break;
-            if (tid == 0 && c == 0) PHB_TRACE_EV(p.trace_id, 7);
-            if (tid == 0 && c == nchunks - 1) PHB_TRACE_EV(p.trace_id, 14);
             const int q = c * p.pp + jp;
             if (act && q < rows_g) {
                 const uint8_t* unit = smem + p.wgu_off + (static_cast<size_t>(c) * p.pp * 2 + mat * p.pp + jp) * p.rb_in +
@@ -289,7 +283,6 @@ __global__ void __launch_bounds__(kTokThreads, 1) moe_token_kernel(const __grid_
             }
         }
     }
-    if (tid == 0) PHB_TRACE_EV(p.trace_id, 8);
     consumer_sync<kTokNC>();  // every dot is done: the gate/up weights' shared memory is free
     {
         // eight lanes per row pair, four row pairs per warp: lanes 0-3 of a
@@ -361,19 +354,15 @@ __global__ void __launch_bounds__(kTokThreads, 1) moe_token_kernel(const __grid_
     const int r = pos2 / sh_ff, hh = pos2 - r * sh_ff;
     const bool act2 = pos2 < p2;
     const bool okd = mbar_wait_warp(full_d, 0, &g_dev_err);
-    if (tid == 0) PHB_TRACE_EV(p.trace_id, 9);
     if (okd && act2) {
         float xr[128];
         const float xf = load_xr_scaled(hs + (r * sh_ff + hh) * (kXPadEvery + kXPad), xr);
-        if (tid == 0) PHB_TRACE_EV(p.trace_id, 10);
         for (int nl = jr; nl < rows_d; nl += rpass) {
             const uint8_t* unit = smem + p.wd_off + (static_cast<size_t>(r) * p.rd + nl) * p.rb_ff + (hh >> 1) * kUB;
             part[(nl * p.K + r) * sh_ff + hh] = half_dot<QT>(unit, hh & 1, xr, xf);
         }
-        if (tid == 0) PHB_TRACE_EV(p.trace_id, 11);
     }
     consumer_sync<kTokNC>();
-    if (tid == 0) PHB_TRACE_EV(p.trace_id, 12);
     // one warp per output row: lane r adds slot r's half-unit sums in order
     // (y_pair), then the slots are combined in ascending order
     for (int nl = warp; nl < rows_d; nl += kTokCW) {
