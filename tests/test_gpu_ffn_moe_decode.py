@@ -108,6 +108,9 @@ MOE_CASES = [
     ("q4_k", 1, 64, 6, 1024, 512),     # one-token kernel: 22 row pairs per chunk, six slots
     ("q8_0", 1, 40, 3, 768, 256),      # one-token kernel: odd unit count, three slots
     ("q4_k", 1, 256, 8, 2048, 1024),   # one-token kernel: 256 experts, five chunks per CTA
+    ("q4_k", 1, 6, 1, 512, 256),       # one-token kernel: top-1
+    ("q4_k", 1, 64, 4, 4096, 1024),    # one-token kernel: a row pair spans two warps, six chunks
+    ("q8_0", 1, 32, 2, 4096, 512),     # one-token kernel: Q8_0 rows of 16 units
 ]
 
 
