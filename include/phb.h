@@ -151,11 +151,15 @@ phb_status phb_ffn_swiglu(int qtype, const void* Wgate, const void* Wup, const v
  * Y: [n_tokens][d_model]. out_idx ([n_tokens][top_k] int32) and out_p
  * ([n_tokens][top_k] fp32) receive the routing in descending logit order
  * when not NULL. n_tokens 1..64, n_experts 1..256, top_k 1..min(8, n_experts).
- * The workspace carries per-row-tile counters (one or two tokens: the last
- * CTA of a tile combines the slots): zero it before the first call and pass
- * the same, otherwise untouched, workspace to later calls (each call returns
- * the counters to zero); calls sharing a workspace must not overlap on the
- * GPU. After a device error (phb_device_error) zero it again.
+ * The workspace carries state between calls: per-row-tile counters (two
+ * tokens: the last CTA of a tile combines the slots; each call returns them
+ * to zero) and, for one token, a call epoch and epoch-tagged copies of the
+ * expert activations (one cooperative kernel exchanges them between its
+ * CTAs). A workspace belongs to one shape (n_tokens, d_model, d_ff,
+ * n_experts, top_k): zero it before its first call and pass it, otherwise
+ * untouched, to later calls of that shape; calls sharing a workspace must
+ * not overlap on the GPU. After a device error (phb_device_error) zero it
+ * again.
  * Once the call has run (stream order), ws begins with the per-pair expert
  * outputs FFN_{e_{t,k}}(X[t]) as [n_tokens * top_k][d_model] fp32 (pair
  * t * top_k + k), followed, at the next multiple of 256 bytes, by their
