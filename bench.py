@@ -313,6 +313,39 @@ def bench_moe(t_tokens, steps, seed):
             "ms_per_step": ms, "bytes": b, "gbs": b / (ms * 1e-3) / 1e9, "tok_per_s": t_tokens / (ms * 1e-3)}
 
 
+_HOST_LINK = {}
+
+
+def host_link_gbs():
+    """Measured host->device rate of the copy engines on this machine: 256 MB of pinned host memory as four
+    concurrent 64 MB copies on four streams, best of five. Context for the tiered-expert row's host
+    traffic, not its bound: the fetch kernel reads host memory with SM loads, which measured faster
+    (~520 GB/s for a 10.6 MB fetch alone)."""
+    if "gbs" not in _HOST_LINK:
+        import torch
+        n, parts = 256 << 20, 4
+        src = torch.empty(n, dtype=torch.uint8).pin_memory()
+        dst = torch.empty(n, dtype=torch.uint8, device="cuda")
+        streams = [torch.cuda.Stream() for _ in range(parts)]
+        best = float("inf")
+        for _ in range(5):
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for i, st in enumerate(streams):
+                st.wait_event(a)
+                with torch.cuda.stream(st):
+                    dst[i * n // parts:(i + 1) * n // parts].copy_(src[i * n // parts:(i + 1) * n // parts],
+                                                                   non_blocking=True)
+            for st in streams:
+                torch.cuda.current_stream().wait_stream(st)
+            b.record()
+            torch.cuda.synchronize()
+            best = min(best, a.elapsed_time(b))
+        _HOST_LINK["gbs"] = n / (best * 1e-3) / 1e9
+    return _HOST_LINK["gbs"]
+
+
 def bench_moe_tiered(t_tokens, steps, seed, n_layers=8, resident=0.5):
     """The MoE layer with only part of the experts resident: a device cache of `resident` x 128
     experts per layer, the rest in pinned host memory read by the GPU (phb_moe_ffn_tiered)."""
@@ -361,6 +394,7 @@ def bench_moe_tiered(t_tokens, steps, seed, n_layers=8, resident=0.5):
             "distinct_experts_per_layer": distinct / n_layers, "from_host_per_layer": from_host / n_layers,
             "ms_per_step": ms, "us_per_layer": ms * 1e3 / n_layers, "bytes": b, "gbs": b / (ms * 1e-3) / 1e9,
             "host_bytes": from_host * per_expert, "host_gbs": from_host * per_expert / (ms * 1e-3) / 1e9,
+            "host_copy_gbs": host_link_gbs(),
             "note": "experts read from host memory are copied over the host link into staging slots, then "
                     "streamed from HBM like the resident ones; GB/s counts every active expert's bytes once"}
 
