@@ -18,9 +18,14 @@
 //  - one thread issues four tcgen05.mma (M128 N256 K16, A in TMEM, B in
 //    shared memory) and commits them to the stage's "empty" barrier;
 // after the last K block the four producer warps drain the accumulator
-// (tcgen05.ld, one TMEM lane per weight row) and write Y, or a split-K
-// partial that a second kernel reduces in split order. X is cast to bf16
-// (round to nearest even) by a first kernel into the caller's workspace.
+// (tcgen05.ld, one TMEM lane per weight row) and write Y. With K split
+// over several CTAs (fewer tiles than SMs), the splits of a tile form one
+// thread-block cluster: each drains its partial tile into its own shared
+// memory and, after a cluster barrier, sums a share of the tile's tokens
+// over the splits' shared memory (in split order) and writes Y. Splits
+// beyond a portable cluster write partials that a second kernel reduces in
+// split order. X is cast to bf16 (round to nearest even) by a first kernel
+// into the caller's workspace.
 //
 // Every wait is bounded; a wait that runs out sets this translation unit's
 // device error word, the kernel drains and frees its TMEM and returns.
@@ -28,6 +33,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "gemv_core.cuh"
@@ -90,7 +96,8 @@ struct PrefillParams {
     int units_per_split;  // 256-weight units of K per split
     int n_units;          // K / 256
     float* y;             // [m][n]
-    float* part;          // [splits][m][n] when gridDim.z > 1
+    float* part;          // [splits][m][n] when gridDim.z > 1 and the splits are not a cluster
+    int cluster;          // 1: the gridDim.z splits of a tile are one cluster (sum over shared memory)
 };
 
 // ---------------------------------------------------------------- tcgen05 / TMA PTX
@@ -137,6 +144,31 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
             smem_addr(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
         : "memory");
+}
+
+// ---------------------------------------------------------------- cluster / distributed shared memory
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA of the cluster: release this CTA's shared-memory
+// writes, then acquire the others'.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// 16 bytes at shared address `addr` of the cluster's CTA `rank`.
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr, uint32_t rank) {
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(addr), "r"(rank));
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(ra)
+                 : "memory");
+    return v;
 }
 
 // 32 consecutive TMEM columns of this warp's 32 lanes, one lane per thread.
@@ -430,7 +462,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---------------- epilogue: warps 0-3 drain TMEM lanes 0..127 (one weight row each)
-    if (warp < kProducerWarps) {
+    if (p.cluster) {
+        // this split's partial tile into shared memory as [256 tokens][128 rows]
+        // fp32 (the token-tile stages are idle once every MMA has completed)
+        float* sAcc = reinterpret_cast<float*>(sB);
+        if (warp < kProducerWarps) {
+            const bool ready = mbar_wait_warp(accb, 0, &g_dev_err_prefill);
+            tc_fence_after();
+            if (ready && !*abort_flag) {
+                const int r = 32 * warp + lane;
+#pragma unroll 1
+                for (int c0 = 0; c0 < kBN; c0 += 32) {
+                    float v[32];
+                    tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + c0, v);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) sAcc[(c0 + j) * kBM + r] = v[j];
+                }
+            }
+        }
+        tc_fence_before();
+        cluster_sync_all();
+        // this CTA's share of the tile's tokens: the splits' partials summed in
+        // split order, 4 rows a thread, one token per warp pass
+        pdl_wait();  // outputs may still be read by the previous kernel
+        const int nsplit = static_cast<int>(gridDim.z);
+        const int per = (kBN + nsplit - 1) / nsplit;
+        const int rank = static_cast<int>(cluster_rank());
+        const int ta = rank * per, tb = min(kBN, min(ta + per, static_cast<int>(p.m - t0)));
+        const uint32_t base = smem_addr(sAcc);
+        for (int it = ta * (kBM / 4) + tid; it < tb * (kBM / 4); it += kThreads) {
+            const int t = it / (kBM / 4), r4 = 4 * (it % (kBM / 4));
+            const uint32_t off = base + static_cast<uint32_t>((t * kBM + r4) * sizeof(float));
+            float4 acc = ld_dsmem_f4(off, 0);
+            for (int q = 1; q < nsplit; ++q) {
+                const float4 v = ld_dsmem_f4(off, static_cast<uint32_t>(q));
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+            }
+            *reinterpret_cast<float4*>(p.y + static_cast<int64_t>(t0 + t) * p.n + n0 + r4) = acc;
+        }
+        // no CTA may leave while another still reads its shared memory
+        cluster_sync_all();
+    } else if (warp < kProducerWarps) {
         pdl_wait();  // outputs may still be read by the previous kernel
         const bool ready = mbar_wait_warp(accb, 0, &g_dev_err_prefill);
         tc_fence_after();
@@ -509,16 +584,50 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 struct SplitPlan {
     int splits;
     int units_per_split;
+    bool cluster;  // the splits of a tile run as one cluster and sum in shared memory
 };
 
-SplitPlan plan_splits(int64_t m, int64_t n, int64_t k) {
+constexpr int kMaxClusterSplits = 8;  // portable cluster size
+
+// Whether clusters of `splits` CTAs of this kernel can be resident (queried once per size).
+template <int QT>
+bool cluster_fits(int splits) {
+    static std::atomic<int> known[kMaxClusterSplits + 1] = {};
+    int v = known[splits].load(std::memory_order_acquire);
+    if (v != 0) return v > 0;
+    constexpr auto kern = prefill_gemm_kernel<QT>;
+    int n = 0;
+    if (ensure_smem_attr<kern>() == cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1, 1, static_cast<unsigned>(splits));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = PCfg<QT>::smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = static_cast<unsigned>(splits);
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+            (void)cudaGetLastError();
+            n = 0;
+        }
+    }
+    known[splits].store(n > 0 ? 1 : -1, std::memory_order_release);
+    return n > 0;
+}
+
+SplitPlan plan_splits(int qt, int64_t m, int64_t n, int64_t k) {
     const int n_units = static_cast<int>(k / kUnitWeights);
     const int64_t tiles = (n / kBM) * ((m + kBN - 1) / kBN);
     const int sms = device_sm_count();
     int splits = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(sms / std::max<int64_t>(1, tiles), n_units)));
     const int ups = (n_units + splits - 1) / splits;
     splits = (n_units + ups - 1) / ups;
-    return {splits, ups};
+    const bool cluster = splits > 1 && splits <= kMaxClusterSplits &&
+                         (qt == 0 ? cluster_fits<0>(splits) : cluster_fits<1>(splits));
+    return {splits, ups, cluster};
 }
 
 inline size_t align_up(size_t v) { return (v + 255) & ~size_t{255}; }
@@ -526,16 +635,16 @@ inline size_t align_up(size_t v) { return (v + 255) & ~size_t{255}; }
 }  // namespace
 
 size_t prefill_ws_bytes(const PrefillReq& q) {
-    const SplitPlan sp = plan_splits(q.m, q.n, q.k);
+    const SplitPlan sp = plan_splits(q.qt, q.m, q.n, q.k);
     size_t b = align_up(static_cast<size_t>(q.m) * q.k * 2);
-    if (sp.splits > 1) b += static_cast<size_t>(sp.splits) * q.m * q.n * sizeof(float);
+    if (sp.splits > 1 && !sp.cluster) b += static_cast<size_t>(sp.splits) * q.m * q.n * sizeof(float);
     return b;
 }
 
 cudaError_t prefill_run(const PrefillReq& q, cudaStream_t s) {
     PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode_fn();
     if (encode == nullptr) return cudaErrorNotSupported;
-    const SplitPlan sp = plan_splits(q.m, q.n, q.k);
+    const SplitPlan sp = plan_splits(q.qt, q.m, q.n, q.k);
     auto* ws = static_cast<uint8_t*>(q.ws);
     uint32_t* xb = reinterpret_cast<uint32_t*>(ws);
     float* part = reinterpret_cast<float*>(ws + align_up(static_cast<size_t>(q.m) * q.k * 2));
@@ -582,18 +691,33 @@ cudaError_t prefill_run(const PrefillReq& q, cudaStream_t s) {
     p.n_units = static_cast<int>(q.k / kUnitWeights);
     p.y = q.y;
     p.part = part;
-    const dim3 grid(static_cast<unsigned>(q.n / kBM), static_cast<unsigned>((q.m + kBN - 1) / kBN),
-                    static_cast<unsigned>(sp.splits));
+    p.cluster = sp.cluster ? 1 : 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(q.n / kBM), static_cast<unsigned>((q.m + kBN - 1) / kBN),
+                       static_cast<unsigned>(sp.splits));
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = static_cast<unsigned>(sp.splits);
+    cfg.attrs = attr;
+    cfg.numAttrs = sp.cluster ? 2 : 1;
     if (q.qt == 0) {
         constexpr auto kern = prefill_gemm_kernel<0>;
         if ((e = ensure_smem_attr<kern>()) != cudaSuccess) return e;
-        e = launch_kernel(kern, grid, dim3(kThreads), PCfg<0>::smem, s, true, tmap, tmap_w, p);
+        cfg.dynamicSmemBytes = PCfg<0>::smem;
+        e = cudaLaunchKernelEx(&cfg, kern, tmap, tmap_w, p);
     } else {
         constexpr auto kern = prefill_gemm_kernel<1>;
         if ((e = ensure_smem_attr<kern>()) != cudaSuccess) return e;
-        e = launch_kernel(kern, grid, dim3(kThreads), PCfg<1>::smem, s, true, tmap, tmap_w, p);
+        cfg.dynamicSmemBytes = PCfg<1>::smem;
+        e = cudaLaunchKernelEx(&cfg, kern, tmap, tmap_w, p);
     }
-    if (e != cudaSuccess || sp.splits == 1) return e;
+    if (e != cudaSuccess || sp.splits == 1 || sp.cluster) return e;
     const int64_t count4 = q.m * q.n / 4;
     return launch_kernel(prefill_reduce_kernel,
                          dim3(static_cast<unsigned>(std::min<int64_t>((count4 + 255) / 256,

@@ -25,11 +25,14 @@ def _built():
 
 CASES = [
     ("q8_0", 64, 128, 256),      # one tile, one K unit
-    ("q4_k", 256, 128, 512),
-    ("q4_k", 300, 256, 1024),    # ragged tokens, split-K across 4 units
-    ("q8_0", 513, 384, 2048),    # ragged tokens past two tiles
-    ("q4_k", 512, 9728, 2560),   # prompt-processing workload: 2560 -> 9728
-    ("q8_0", 512, 2560, 9728),   # 9728 -> 2560 (split-K)
+    ("q4_k", 256, 128, 512),     # one tile, K split over a cluster of 2
+    ("q4_k", 300, 256, 1024),    # ragged tokens; a cluster of 4 splits per tile
+    ("q8_0", 513, 384, 2048),    # ragged tokens past two tiles; clusters of 8
+    ("q4_k", 300, 1280, 5120),   # clusters of 7 splits of 3 units (the last split 2)
+    ("q8_0", 200, 1280, 4864),   # 10 splits: partials summed by the reduction kernel
+    ("q4_k", 128, 768, 8192),    # 16 splits, one token tile of 128
+    ("q4_k", 512, 9728, 2560),   # prompt-processing workload: 2560 -> 9728 (one tile per SM)
+    ("q8_0", 512, 2560, 9728),   # 9728 -> 2560: clusters of 3 splits
 ]
 
 
@@ -65,8 +68,9 @@ def test_prefill_identity_like_weights_exact():
     assert np.array_equal(y.astype(np.float64), oracle.round_to_bf16(x))
 
 
-def test_prefill_deterministic():
-    qtype, m, n, k = "q4_k", 300, 256, 1024
+@pytest.mark.parametrize("qtype,m,n,k", [("q4_k", 300, 256, 1024), ("q4_k", 300, 1280, 5120),
+                                         ("q8_0", 200, 1280, 4864)])
+def test_prefill_deterministic(qtype, m, n, k):
     blob = to_dev(synth.blocks(qtype, 720, 0, n, k))
     x = to_dev(synth.normal_f32(720, 1, (m, k)))
     a = to_host(phb.gemm_q_prefill(qtype, blob, x, n, k))
