@@ -9,6 +9,7 @@ workload shapes, against the exact fp32-operand product under the
 
 import numpy as np
 import pytest
+import torch
 
 import oracle
 import quantized_decode_gguf_gb300 as phb
@@ -33,6 +34,7 @@ CASES = [
     ("q4_k", 128, 768, 8192),    # 16 splits, one token tile of 128
     ("q4_k", 512, 9728, 2560),   # prompt-processing workload: 2560 -> 9728 (one tile per SM)
     ("q8_0", 512, 2560, 9728),   # 9728 -> 2560: clusters of 3 splits
+    ("q8_0", 600, 9728, 512),    # 228 tiles: two waves of CTAs, ragged tokens
 ]
 
 
@@ -76,3 +78,22 @@ def test_prefill_deterministic(qtype, m, n, k):
     a = to_host(phb.gemm_q_prefill(qtype, blob, x, n, k))
     b = to_host(phb.gemm_q_prefill(qtype, blob, x, n, k))
     assert np.array_equal(a, b)
+
+
+def test_prefill_workspace_reused_across_shapes():
+    # one workspace serves calls of different grids and split plans; results
+    # equal fresh-workspace ones
+    shapes = [("q4_k", 300, 1280, 5120), ("q8_0", 512, 2560, 9728), ("q4_k", 64, 128, 256),
+              ("q8_0", 512, 9728, 2560), ("q8_0", 200, 1280, 4864), ("q4_k", 600, 9728, 512)]
+    size = max(phb.prefill_workspace_size(*shape) for shape in shapes)
+    ws = torch.zeros(size, dtype=torch.uint8, device="cuda")
+    inputs = []
+    for i, (qtype, m, n, k) in enumerate(shapes):
+        blob = to_dev(synth.blocks(qtype, 730 + i, 0, n, k))
+        x = to_dev(synth.normal_f32(730 + i, 1, (m, k)))
+        inputs.append((qtype, m, n, k, blob, x, to_host(phb.gemm_q_prefill(qtype, blob, x, n, k))))
+    for _ in range(2):
+        for qtype, m, n, k, blob, x, ref in inputs:
+            y = to_host(phb.gemm_q_prefill(qtype, blob, x, n, k, ws=ws))
+            assert np.array_equal(y, ref), (qtype, m, n, k)
+    check_device_clean()
