@@ -17,13 +17,7 @@ cudaError_t read_dev_err_decode(int* code) {
     return e;
 }
 
-#ifdef PHB_TRACE
-// Debug builds only: copy out the per-CTA timestamps of the decode kernels.
-extern "C" int phb_trace_read(void* dst, size_t bytes) {
-    if (bytes > sizeof(g_trace)) bytes = sizeof(g_trace);
-    return static_cast<int>(cudaMemcpyFromSymbol(dst, g_trace, bytes));
-}
-#endif
+PHB_TRACE_READER(phb_trace_read)  // debug builds: the decode kernels' stamps
 
 template <int QT>
 static cudaError_t decode_dispatch(const GemvReq& q, const GemvPlan& pl, cudaStream_t s) {

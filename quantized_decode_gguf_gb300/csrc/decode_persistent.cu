@@ -37,20 +37,6 @@
 #include <algorithm>
 #include <cstdint>
 
-#ifdef PHB_TRACE
-// Debug builds only: per-stage times of the first CTAs [cta][stage][issued, ready, wait start].
-constexpr int kStTraceCtas = 4, kStTraceStages = 512;
-static __device__ unsigned long long g_stage_trace[kStTraceCtas * kStTraceStages * 3];
-#define PHB_STAGE_HOOK(kind, s)                                                                       \
-    do {                                                                                              \
-        if (blockIdx.x < kStTraceCtas && (s) < kStTraceStages) {                                      \
-            unsigned long long t_;                                                                    \
-            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                                    \
-            g_stage_trace[(blockIdx.x * kStTraceStages + (s)) * 3 + (kind)] = t_;                      \
-        }                                                                                             \
-    } while (0)
-#endif
-
 #include "gemv_plan.cuh"
 #include "persist_common.cuh"
 #include "phb_internal.h"
@@ -67,16 +53,7 @@ cudaError_t read_dev_err_decode_persistent(int* code) {
     return e;
 }
 
-#ifdef PHB_TRACE
-extern "C" int phb_trace_read_persistent(void* dst, size_t bytes) {
-    if (bytes > sizeof(g_trace)) bytes = sizeof(g_trace);
-    return static_cast<int>(cudaMemcpyFromSymbol(dst, g_trace, bytes));
-}
-extern "C" int phb_trace_read_stages(void* dst, size_t bytes) {
-    if (bytes > sizeof(g_stage_trace)) bytes = sizeof(g_stage_trace);
-    return static_cast<int>(cudaMemcpyFromSymbol(dst, g_stage_trace, bytes));
-}
-#endif
+PHB_TRACE_READER(phb_trace_read_persistent)
 
 namespace {
 
@@ -117,11 +94,6 @@ __global__ void __launch_bounds__(KCfg<QT, kCW>::threads, 1) decode_persistent_k
     float* xfac = reinterpret_cast<float*>(empty + C::ns);
     float* red = xfac + kAccStride;
     int* flag = reinterpret_cast<int*>(red + (2 * kMaxConsumerWarps + 3) * kAccStride);
-#ifdef PHB_TRACE
-    int* retries = flag + 1;  // debug builds: re-read rounds of the staging pass
-#else
-    int* retries = nullptr;
-#endif
 
     const int tid = threadIdx.x;
     const int nctas = gridDim.x;
@@ -134,7 +106,6 @@ __global__ void __launch_bounds__(KCfg<QT, kCW>::threads, 1) decode_persistent_k
         }
         fence_barrier_init();
         *flag = 0;
-        if (retries != nullptr) *retries = 0;
     }
     __syncthreads();
     const unsigned epoch = ld_relaxed(p.state + 2);
@@ -213,21 +184,21 @@ __global__ void __launch_bounds__(KCfg<QT, kCW>::threads, 1) decode_persistent_k
             switch (j) {
                 case 0:
                     ok = stage_vec<1>(sctx, lin_t, lin_p, tag_lin, kseg, xs, xfac, red, flag, nullptr, nullptr, 0,
-                                      res, 0, retries, op);
+                                      res, 0, op);
                     break;
                 case 1:
                     ok = stage_vec<2>(sctx, p.qkv + rep * p.rs_qkv, nullptr, tag_prev, kseg, xs, xfac, red, flag,
                                       lin_t ? lin_t + row0 : nullptr, lin_p ? lin_p + row0 : nullptr, tag_lin, res,
-                                      t.rows_here, retries, op);
+                                      t.rows_here, op);
                     break;
                 case 2:
                     ok = stage_vec<1>(sctx, p.x1 + rep * p.rs_dm, nullptr, tag_prev, kseg, xs, xfac, red, flag, nullptr, nullptr, 0,
-                                      res, 0, retries, op);
+                                      res, 0, op);
                     break;
                 default:
                     ok = stage_vec<0>(sctx, p.act + rep * p.rs_ff, nullptr, tag_prev, kseg, xs, xfac, red, flag,
                                       p.x1 + rep * p.rs_dm + row0,
-                                      nullptr, tag_me - 2, res, t.rows_here, retries, op);
+                                      nullptr, tag_me - 2, res, t.rows_here, op);
                     break;
             }
             alive = ok;

@@ -30,32 +30,12 @@
 
 #include "gemv_core.cuh"
 #include "phb_common.cuh"
+#include "trace.cuh"
 
 namespace phb {
 
 // Device error word of the translation unit that includes this header.
 static __device__ int g_dev_err;
-
-#ifdef PHB_TRACE
-// Debug builds only: per-CTA timestamps [launch id][cta][event].
-constexpr int kTraceLaunches = 128, kTraceCtas = 160, kTraceEvents = 16;
-static __device__ uint64_t g_trace[kTraceLaunches * kTraceCtas * kTraceEvents];
-#define PHB_TRACE_EV(id, ev)                                                                          \
-    do {                                                                                              \
-        if ((id) >= 0 && (id) < kTraceLaunches && blockIdx.x < kTraceCtas && blockIdx.y == 0)          \
-            g_trace[((id) * kTraceCtas + blockIdx.x) * kTraceEvents + (ev)] = global_timer_ns();        \
-    } while (0)
-#else
-#define PHB_TRACE_EV(id, ev) \
-    do {                     \
-    } while (0)
-#endif
-
-#ifndef PHB_STAGE_HOOK
-#define PHB_STAGE_HOOK(kind, s) \
-    do {                        \
-    } while (0)
-#endif
 
 enum XMode : int { kXPlain = 0, kXRmsNorm = 1, kXGatherV = 2, kXRowList = 3 };
 enum Epi : int { kEpiStore = 0, kEpiResid = 1, kEpiSwiGLU = 2 };
@@ -129,7 +109,6 @@ __device__ __forceinline__ bool produce_tile(const Tile& t, int nmat, uint8_t* s
         const int slot = s % C::ns;
         if (s >= C::ns && !mbar_wait(&empty[slot], ((s / C::ns) - 1) & 1, &g_dev_err)) return false;
         const int g1 = min(units, g0 + stage_units);
-        PHB_STAGE_HOOK(0, s);
         mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>((g1 - g0) * C::ub));
         uint8_t* dst = stages + slot * C::stage_bytes;
         if (flat) {
@@ -172,12 +151,10 @@ __device__ __forceinline__ bool consume_tile(const Tile& t, int mode, const uint
     const int seg_half = 2 * t.useg;  // half units per row segment
     for (int g0 = 0; g0 < units; g0 += C::stage_units, ++s) {
         const int slot = s % C::ns;
-        if (threadIdx.x == 0) PHB_STAGE_HOOK(2, s);
         if (!mbar_wait_warp(&full[slot], (s / C::ns) & 1, &g_dev_err)) {
             mbar_wait(&full[slot], (s / C::ns) & 1, &g_dev_err);  // second bounded wait for the copy in flight
             return false;
         }
-        if (threadIdx.x == 0) PHB_STAGE_HOOK(1, s);
         const int g = g0 + ulocal;
         const int segi = g / t.useg;
         const int u = g - segi * t.useg;
@@ -549,12 +526,6 @@ __global__ void __launch_bounds__(KCfg<QT, CW>::threads, MAXB <= 2 ? 2 : 1)
         }
     };
     int s = 0;
-#ifdef PHB_TRACE
-    if (tid == 0) {
-        mbar_wait(&full[0], 0, &g_dev_err);
-        PHB_TRACE_EV(p.trace_id, 3);
-    }
-#endif
     consume_tile<QT, CW, MAXB, NMAT>(t, p.sum_mode, smem, full, empty, s, xs, xpad_len(kseg), xfac, batch, part,
                                      row_acc, epi);
     if (tid == 0) PHB_TRACE_EV(p.trace_id, 4);

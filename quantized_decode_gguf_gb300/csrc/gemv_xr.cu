@@ -37,13 +37,7 @@ cudaError_t read_dev_err_gemv_xr(int* code) {
     return e;
 }
 
-#ifdef PHB_TRACE
-// Debug builds only: copy out this unit's per-CTA timestamps.
-extern "C" int phb_trace_read_gemv_xr(void* dst, size_t bytes) {
-    if (bytes > sizeof(g_trace)) bytes = sizeof(g_trace);
-    return static_cast<int>(cudaMemcpyFromSymbol(dst, g_trace, bytes));
-}
-#endif
+PHB_TRACE_READER(phb_trace_read_gemv_xr)
 
 namespace {
 

@@ -51,12 +51,7 @@ cudaError_t read_dev_err_moe(int* code) {
     return e;
 }
 
-#ifdef PHB_TRACE
-extern "C" int phb_trace_read_moe(void* dst, size_t bytes) {
-    if (bytes > sizeof(g_trace)) bytes = sizeof(g_trace);
-    return static_cast<int>(cudaMemcpyFromSymbol(dst, g_trace, bytes));
-}
-#endif
+PHB_TRACE_READER(phb_trace_read_moe)
 
 namespace {
 

@@ -54,13 +54,7 @@ cudaError_t read_dev_err_moe_token(int* code) {
     return e;
 }
 
-#ifdef PHB_TRACE
-// Debug builds only: copy out this unit's per-CTA timestamps.
-extern "C" int phb_trace_read_moe_token(void* dst, size_t bytes) {
-    if (bytes > sizeof(g_trace)) bytes = sizeof(g_trace);
-    return static_cast<int>(cudaMemcpyFromSymbol(dst, g_trace, bytes));
-}
-#endif
+PHB_TRACE_READER(phb_trace_read_moe_token)
 
 namespace {
 

@@ -125,9 +125,8 @@ template <int XMODE>
 __device__ __forceinline__ bool stage_vec(const StageCtx& p, const uint2* src_t, const float* src_p, unsigned tag,
                                           int kseg, float* xs, float* xfac, float* red, int* flag,
                                           const uint2* res_t, const float* res_p, unsigned res_tag, float* res_dst,
-                                          int nres, int* retries, int trace_op) {
+                                          int nres, int trace_op) {
     (void)trace_op;
-    (void)retries;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n4 = kseg / 4;  // a multiple of 64
     bool ok = true;
@@ -159,14 +158,6 @@ __device__ __forceinline__ bool stage_vec(const StageCtx& p, const uint2* src_t,
                     miss |= 1u << i;
             }
         }
-#ifdef PHB_TRACE
-        if (tid == 0 && base == 0) {
-            float chk = v[0].x;  // wait for the first pass's data
-            asm volatile("" ::"f"(chk));
-            if (miss == 0) PHB_TRACE_EV(trace_op, 8);
-        }
-        if (miss != 0 && retries != nullptr) atomicAdd(retries, 1);
-#endif
         if (miss != 0) {
             // some pairs were not yet current: re-read those (bounded)
             WaitClock clk;
@@ -230,13 +221,6 @@ __device__ __forceinline__ bool stage_vec(const StageCtx& p, const uint2* src_t,
         red[kCW + warp] = ssq;
     }
     consumer_sync<kNC>();
-#ifdef PHB_TRACE
-    if (tid == 0) {
-        if (trace_op < kTraceLaunches && blockIdx.x < kTraceCtas)
-            g_trace[(trace_op * kTraceCtas + blockIdx.x) * kTraceEvents + 9] = static_cast<uint64_t>(*retries);
-        *retries = 0;
-    }
-#endif
     if (tid == 0) PHB_TRACE_EV(trace_op, 5);
     // every thread derives the same scale from the per-warp partials
     float m = 0.f, sq = 0.f;
@@ -302,12 +286,10 @@ __device__ __forceinline__ bool consume_xr(const Tile& t, int segs, const uint8_
     const int nseg = NMAT * t.rows_here;
     for (int seg0 = 0; seg0 < nseg; seg0 += segs, ++s) {
         const int slot = s % C::ns;
-        if (threadIdx.x == 0) PHB_STAGE_HOOK(2, s);
         if (!stage_wait(&full[slot], (s / C::ns) & 1)) {
             if (lane == 0) mbar_wait(&full[slot], (s / C::ns) & 1, &g_dev_err);  // second bounded wait for the copy
             return false;
         }
-        if (threadIdx.x == 0) PHB_STAGE_HOOK(1, s);
         const int seg = seg0 + j;
         if (compute && j < segs && seg < nseg) {
             const uint8_t* ub = stages + slot * C::stage_bytes + (j * t.useg + (pos >> 1)) * C::ub;

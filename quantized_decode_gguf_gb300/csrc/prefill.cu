@@ -39,31 +39,15 @@
 #include "gemv_core.cuh"
 #include "phb_common.cuh"
 #include "phb_internal.h"
+#include "trace.cuh"
 
 namespace phb {
 
 static __device__ int g_dev_err_prefill;
 
-#ifdef PHB_TRACE
-// Debug builds only: global-timer stamps per CTA of the last GEMM launch
-// (entry, TMEM allocated, first weight tile stored, X ready, first MMA,
-// last MMA issued, accumulator complete, outputs written).
-constexpr int kPfTraceCtas = 160, kPfTraceEvents = 8;
-static __device__ unsigned long long g_pf_trace[kPfTraceCtas * kPfTraceEvents];
-#define PF_TRACE(ev)                                                                                   \
-    do {                                                                                               \
-        const unsigned c_ = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);            \
-        if (c_ < kPfTraceCtas) g_pf_trace[c_ * kPfTraceEvents + (ev)] = global_timer_ns();              \
-    } while (0)
-extern "C" int phb_trace_read_prefill(void* dst, size_t bytes) {
-    if (bytes > sizeof(g_pf_trace)) bytes = sizeof(g_pf_trace);
-    return static_cast<int>(cudaMemcpyFromSymbol(dst, g_pf_trace, bytes));
-}
-#else
-#define PF_TRACE(ev) \
-    do {             \
-    } while (0)
-#endif
+// debug builds: stamps of the last GEMM launch per CTA (entry, TMEM allocated, first
+// weight tile stored, X ready, first MMA, last MMA issued, accumulator complete, outputs written)
+PHB_TRACE_READER(phb_trace_read_prefill)
 
 cudaError_t read_dev_err_prefill(int* code) {
     int v = 0;
@@ -326,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (tid == 0) PF_TRACE(0);
+    if (tid == 0) PHB_TRACE_EV(0, 0);
     const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kBM;
     const int t0 = blockIdx.y * kBN;
     const int split = blockIdx.z;
@@ -357,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    if (tid == 0) PF_TRACE(1);
+    if (tid == 0) PHB_TRACE_EV(0, 1);
     pdl_launch_dependents();
 
     if (warp < kProducerWarps * kProducerGroups) {
@@ -419,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&full[s]);
-                if (tid == 0 && i == 0) PF_TRACE(2);
+                if (tid == 0 && i == 0) PHB_TRACE_EV(0, 2);
             }
             if (*abort_flag) break;
             if constexpr (!PCfg<QT>::staged) {
@@ -431,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- token tiles by TMA
         if (lane == 0) {
             pdl_wait();  // the bf16 copy of X comes from the previous kernel
-            PF_TRACE(3);
+            PHB_TRACE_EV(0, 3);
             for (int i = 0; i < nkb; ++i) {
                 const int s = i % kStages;
                 if (i >= kStages && !mbar_wait(&empty[s], ((i / kStages) - 1) & 1, &g_dev_err_prefill)) {
@@ -474,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                if (i == 0) PF_TRACE(4);
+                if (i == 0) PHB_TRACE_EV(0, 4);
 #pragma unroll
                 for (int kk = 0; kk < kBK / 16; ++kk) {
                     const uint64_t bd = smem_desc_sw128(sB + s * kBTile + kk * 32);
@@ -483,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(&empty[s]);
             }
             if (!ok) *abort_flag = 1;
-            PF_TRACE(5);
+            PHB_TRACE_EV(0, 5);
             mma_commit(accb);  // arrives once every MMA issued above has completed
         }
     }
@@ -495,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* sAcc = reinterpret_cast<float*>(sB);
         if (warp < kProducerWarps) {
             const bool ready = mbar_wait_warp(accb, 0, &g_dev_err_prefill);
-            if (tid == 0) PF_TRACE(6);
+            if (tid == 0) PHB_TRACE_EV(0, 6);
             tc_fence_after();
             if (ready && !*abort_flag) {
                 const int r = 32 * warp + lane;
@@ -533,11 +517,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // no CTA may leave while another still reads its shared memory
         cluster_sync_all();
-        if (tid == 0) PF_TRACE(7);
+        if (tid == 0) PHB_TRACE_EV(0, 7);
     } else if (warp < kProducerWarps) {
         pdl_wait();  // outputs may still be read by the previous kernel
         const bool ready = mbar_wait_warp(accb, 0, &g_dev_err_prefill);
-        if (tid == 0) PF_TRACE(6);
+        if (tid == 0) PHB_TRACE_EV(0, 6);
         tc_fence_after();
         if (ready && !*abort_flag && nkb > 0) {
             const int64_t n = n0 + 32 * warp + lane;
@@ -556,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (tid == 0 && !p.cluster) PF_TRACE(7);
+    if (tid == 0 && !p.cluster) PHB_TRACE_EV(0, 7);
     if (warp == kMmaWarp) {
         // every MMA issued has completed once accb has arrived (bounded wait)
         mbar_wait_warp(accb, 0, &g_dev_err_prefill);
