@@ -285,4 +285,26 @@ __device__ __forceinline__ float dot_q4_k_half_xr(const uint8_t* blk, int h, con
     return ((s2.x + s2.y) + (t2.x + t2.y)) * xfac;
 }
 
+// Sum of a row's n half-unit partials in a fixed order. With n a multiple of
+// four and p 16-byte aligned: four interleaved sums over 16-byte loads
+// (partials i, i + 4, ... in sum i % 4), combined as (s0 + s1) + (s2 + s3);
+// otherwise one sum in index order. Either way the order depends only on n,
+// so results are reproducible.
+__device__ __forceinline__ float row_sum(const float* p, int n) {
+    if ((n & 3) == 0 && (reinterpret_cast<uintptr_t>(p) & 15) == 0) {
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = 0; i < n; i += 4) {
+            const float4 v = *reinterpret_cast<const float4*>(p + i);
+            a.x += v.x;
+            a.y += v.y;
+            a.z += v.z;
+            a.w += v.w;
+        }
+        return (a.x + a.y) + (a.z + a.w);
+    }
+    float v = 0.f;
+    for (int i = 0; i < n; ++i) v += p[i];
+    return v;
+}
+
 }  // namespace phb

@@ -147,10 +147,7 @@ __global__ void __launch_bounds__(32 * CW + 32, CW <= 6 ? 2 : 1) gemv_xr_kernel(
         float a[NMAT];
 #pragma unroll
         for (int m = 0; m < NMAT; ++m) {
-            const float* q = part + static_cast<size_t>(r * NMAT + m) * seg_half;
-            float v = 0.f;
-            for (int h = 0; h < seg_half; ++h) v += q[h];
-            a[m] = v;
+            a[m] = row_sum(part + static_cast<size_t>(r * NMAT + m) * seg_half, seg_half);
         }
         p.y[row0 + r] = NMAT == 2 ? silu_mul(a[0], a[NMAT - 1]) : a[0];
     }

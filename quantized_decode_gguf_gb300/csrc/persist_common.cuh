@@ -306,12 +306,10 @@ __device__ __forceinline__ bool consume_xr(const Tile& t, int segs, const uint8_
     if (!compute) return true;
     if (threadIdx.x == 0) PHB_TRACE_EV(trace_op, 7);
     consumer_sync<kNC>();
-    // one thread per (row, matrix) sum, half units in order; the gate/up
+    // one thread per (row, matrix) sum, in row_sum's fixed order; the gate/up
     // pair meets in rsum
     for (int it = tid; it < nseg; it += kNC) {
-        const float* q = part + static_cast<size_t>(it) * seg_half;
-        float v = 0.f;
-        for (int h = 0; h < seg_half; ++h) v += q[h];
+        const float v = row_sum(part + static_cast<size_t>(it) * seg_half, seg_half);
         if constexpr (NMAT == 1)
             epi(it, v, 0.f);
         else
