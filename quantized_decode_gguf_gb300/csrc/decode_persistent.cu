@@ -11,11 +11,15 @@
 //
 // Activations stay in registers. A consumer thread owns one fixed half-unit
 // position (128 consecutive k) of the GEMV's rows and keeps those 128 scaled
-// activations in registers for the whole GEMV, so
-// per weight only the quantized bytes come from shared memory. A stage holds
-// whole row segments: with useg units per row segment, a stage carries
-// floor(128 / (nmat * useg)) * nmat segments and thread t works on segment
-// t / (2 * useg), half unit t % (2 * useg).
+// activations in registers for the whole GEMV, so per weight only the
+// quantized bytes come from shared memory. A stage holds whole row segments:
+// with useg units per row segment, a stage carries
+// floor(176 / (nmat * useg)) * nmat segments (176 = half the consumer
+// threads) and thread t works on segment t % segs at half unit t / segs, so a
+// warp's threads share a few positions and fill their registers mostly by
+// broadcasts. Segments whose length is a multiple of 128 bytes are padded by
+// 16 bytes in the stage, so that the threads' weight reads at one position
+// spread over the shared-memory banks.
 //
 // Readiness travels with the data. Every intermediate vector (qkv, x1, the
 // SwiGLU activation, each layer's output) is stored as 64-bit pairs
@@ -78,6 +82,7 @@ struct PersistParams {
     uint2* xl[2];
     int64_t rs_qkv, rs_dm, rs_ff;  // replica strides (pairs) of qkv, the d_model vectors, act
     unsigned* state;
+    uint32_t stage_stride;         // bytes per ring stage (row segments at padded places)
     uint32_t xs_off, part_off, res_off, bar_off;
 };
 
@@ -145,7 +150,7 @@ __global__ void __launch_bounds__(KCfg<QT, kCW>::threads, 1) decode_persistent_k
                 int nmat, segs;
                 int64_t row0;
                 if (!op_tile(op, t, nmat, row0, segs)) continue;
-                if (!produce_tile<QT, kCW, NS>(t, nmat, smem, full, empty, s, pol, segs * t.useg)) break;
+                if (!produce_segs<QT, NS>(t, nmat, segs, smem, p.stage_stride, full, empty, s, pol)) break;
             }
         }
         return;
@@ -207,7 +212,7 @@ __global__ void __launch_bounds__(KCfg<QT, kCW>::threads, 1) decode_persistent_k
         // this thread's half-unit position: activations into registers
         float xr[kHalfK];
         {
-            const int pos = tid % (2 * t.useg);
+            const int pos = xr_pos(segs, t.useg);
             const float* xp = xs + pos * (kXPadEvery + kXPad);
 #pragma unroll
             for (int i = 0; i < kHalfK; i += 4) {
@@ -219,6 +224,7 @@ __global__ void __launch_bounds__(KCfg<QT, kCW>::threads, 1) decode_persistent_k
             }
         }
         const float xf = xfac[0];
+        if (tid == 0) PHB_TRACE_EV(op, 9);
         const bool last = (l == p.n_layers - 1);
         auto store_all = [&](uint2* buf, int64_t rs, int64_t n, float v) {
 #pragma unroll
@@ -241,9 +247,9 @@ __global__ void __launch_bounds__(KCfg<QT, kCW>::threads, 1) decode_persistent_k
         // on abort the stages are still drained (no copy may be left in flight)
         bool ok;
         if (nmat == 2)
-            ok = consume_xr<QT, 2, NS>(t, segs, smem, full, empty, s, xr, xf, part, rsum, alive, op, epi);
+            ok = consume_xr<QT, 2, NS>(t, segs, smem, p.stage_stride, full, empty, s, xr, xf, part, rsum, alive, op, epi);
         else
-            ok = consume_xr<QT, 1, NS>(t, segs, smem, full, empty, s, xr, xf, part, rsum, alive, op, epi);
+            ok = consume_xr<QT, 1, NS>(t, segs, smem, p.stage_stride, full, empty, s, xr, xf, part, rsum, alive, op, epi);
         alive = alive && ok;
         consumer_sync<kNC>();
         if (tid == 0) {
@@ -377,21 +383,37 @@ cudaError_t decode_persistent_run(int qt, const void* const* wl, int n_layers, i
     const int max_useg = static_cast<int>(kmax / kUnitWeights);
     const int deep = qt == 0 ? Rings<0>::deep : Rings<1>::deep;
     const int shallow = qt == 0 ? Rings<0>::shallow : Rings<1>::shallow;
-    // every op may need tile partials (2 * nmat * rows * useg floats)
-    const size_t tile_part = 2 * 2 * static_cast<size_t>(max_rows) * max_useg * sizeof(float);
+    // a stage holds the widest op's row segments at their padded places;
+    // `part` the largest op's half-unit sums (nmat * rows * 2 useg floats)
+    const int64_t op_n[4] = {p.qkv_dim, d_model, d_ff, d_model};
+    const int64_t op_k[4] = {d_model, p.q_dim, d_model, d_ff};
+    const int op_nmat[4] = {1, 1, 2, 1};
+    size_t stage_stride = 0, part_floats = 0;
+    for (int o = 0; o < 4; ++o) {
+        const int useg = static_cast<int>(op_k[o] / kUnitWeights);
+        const int segs = segs_per_stage(kStageUnits, useg, op_nmat[o]);
+        stage_stride = std::max(stage_stride, static_cast<size_t>(segs) * seg_stride_bytes(useg, ub));
+        const size_t rows = static_cast<size_t>((op_n[o] + grid - 1) / grid);
+        part_floats = std::max(part_floats, static_cast<size_t>(op_nmat[o]) * rows * 2 * useg);
+    }
+    stage_stride = (stage_stride + 127) & ~size_t{127};
+    p.stage_stride = static_cast<uint32_t>(stage_stride);
     int ns = 0;
     size_t smem = 0;
     for (int cand : {deep, shallow}) {
-        const SmemLayout lay = stream_smem_layout(qt, kCW, 2, 1, static_cast<int>(max_rows), max_useg, cand);
-        const size_t res_off = lay.part + tile_part;
+        size_t off = static_cast<size_t>(cand) * stage_stride;
+        const size_t xs_off = off;
+        off += static_cast<size_t>(xpad_len(static_cast<int>(kmax))) * sizeof(float);
+        const size_t part_off = off;
+        const size_t res_off = part_off + part_floats * sizeof(float);
         // residuals (kNC floats) then row sums (2 * max_rows floats)
         const size_t bar_off = (res_off + (kNC + 2 * static_cast<size_t>(max_rows)) * sizeof(float) + 15) & ~size_t{15};
         const size_t total = bar_off + 2 * cand * sizeof(uint64_t) + kTailFloats * sizeof(float);
         if (total > kSmemOptin) continue;
         ns = cand;
         smem = total;
-        p.xs_off = lay.xs;
-        p.part_off = lay.part;
+        p.xs_off = static_cast<uint32_t>(xs_off);
+        p.part_off = static_cast<uint32_t>(part_off);
         p.res_off = static_cast<uint32_t>(res_off);
         p.bar_off = static_cast<uint32_t>(bar_off);
         break;

@@ -268,21 +268,68 @@ __device__ __forceinline__ bool stage_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Row segments (whole rows of one matrix) lie in a stage seg_stride_bytes
+// apart: a segment's bytes, plus 16 when that length is a multiple of 128, so
+// that the segments start in different shared-memory bank groups (the
+// consumers read one half unit of many segments at once).
+__host__ __device__ constexpr int seg_stride_bytes(int useg, int ub) {
+    return useg * ub + (((useg * ub) & 127) == 0 ? 16 : 0);
+}
+
+// This thread's half-unit position within a row segment: consecutive threads
+// take consecutive segments at one position (segments fastest), so a warp's
+// threads share few positions and the register fill of their activations is
+// mostly broadcasts. Threads past segs * 2 useg get the last position (their
+// fill stays in range; they compute nothing).
+__device__ __forceinline__ int xr_pos(int segs, int useg) { return min(static_cast<int>(threadIdx.x) / segs, 2 * useg - 1); }
+
+// Producer of the persistent kernel: the tile's row segments in order, segs
+// per stage (gate and up rows alternate when nmat == 2), each at its padded
+// place; one copy per stage when the rows need no padding.
+template <int QT, int NS>
+__device__ __forceinline__ bool produce_segs(const Tile& t, int nmat, int segs, uint8_t* stages, uint32_t stage_stride,
+                                             uint64_t* full, uint64_t* empty, int& s, uint64_t pol) {
+    using C = KCfg<QT, kCW, NS>;
+    const int nseg = nmat * t.rows_here;
+    const int seg_bytes = t.useg * C::ub;
+    const int ss = seg_stride_bytes(t.useg, C::ub);
+    for (int seg0 = 0; seg0 < nseg; seg0 += segs, ++s) {
+        const int slot = s % C::ns;
+        if (s >= C::ns && !mbar_wait(&empty[slot], ((s / C::ns) - 1) & 1, &g_dev_err)) return false;
+        const int n = min(segs, nseg - seg0);
+        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(n * seg_bytes));
+        uint8_t* dst = stages + static_cast<size_t>(slot) * stage_stride;
+        if (nmat == 1 && ss == seg_bytes) {
+            bulk_g2s_hint(dst, t.w[0] + static_cast<int64_t>(seg0) * t.row_bytes, static_cast<uint32_t>(n * seg_bytes),
+                          &full[slot], pol);
+            continue;
+        }
+        for (int j = 0; j < n; ++j) {
+            const int seg = seg0 + j, r = seg / nmat, mat = seg - r * nmat;
+            bulk_g2s_hint(dst + j * ss, (mat == 0 ? t.w[0] : t.w[1]) + static_cast<int64_t>(r) * t.row_bytes,
+                          static_cast<uint32_t>(seg_bytes), &full[slot], pol);
+        }
+    }
+    return true;
+}
+
 // Consumers, activations in registers: dot every staged half unit of the
-// tile, park the half-unit sums in `part` (2 * NMAT * rows_here * useg
+// tile, park the half-unit sums in `part` (NMAT * rows_here * 2 useg
 // floats) and, once the tile is done, sum each row (one thread per row and
-// matrix, half units in order) and hand it to epi(r, a0, a1) (a1 the up
-// row's sum for NMAT == 2; `rsum` holds NMAT * rows_here floats). Returns
-// false on a wait timeout.
+// matrix, in row_sum's fixed order) and hand it to epi(r, a0, a1) (a1 the up
+// row's sum for NMAT == 2; `rsum` holds NMAT * rows_here floats). Thread t
+// works on segment t % segs at position xr_pos(segs, useg) of every stage.
+// Returns false on a wait timeout.
 template <int QT, int NMAT, int NS, class EpiF>
-__device__ __forceinline__ bool consume_xr(const Tile& t, int segs, const uint8_t* stages, uint64_t* full,
-                                           uint64_t* empty, int& s, const float (&xr)[kHalfK], float xfac, float* part, float* rsum, bool compute, int trace_op,
-                                           EpiF epi) {
+__device__ __forceinline__ bool consume_xr(const Tile& t, int segs, const uint8_t* stages, uint32_t stage_stride,
+                                           uint64_t* full, uint64_t* empty, int& s, const float (&xr)[kHalfK],
+                                           float xfac, float* part, float* rsum, bool compute, int trace_op, EpiF epi) {
     (void)trace_op;
     using C = KCfg<QT, kCW, NS>;
     const int tid = threadIdx.x, lane = tid & 31;
     const int seg_half = 2 * t.useg;
-    const int j = tid / seg_half, pos = tid - j * seg_half;
+    const int j = tid % segs, pos = tid / segs;
+    const int ss = seg_stride_bytes(t.useg, C::ub);
     const int nseg = NMAT * t.rows_here;
     for (int seg0 = 0; seg0 < nseg; seg0 += segs, ++s) {
         const int slot = s % C::ns;
@@ -291,8 +338,8 @@ __device__ __forceinline__ bool consume_xr(const Tile& t, int segs, const uint8_
             return false;
         }
         const int seg = seg0 + j;
-        if (compute && j < segs && seg < nseg) {
-            const uint8_t* ub = stages + slot * C::stage_bytes + (j * t.useg + (pos >> 1)) * C::ub;
+        if (compute && pos < seg_half && seg < nseg) {
+            const uint8_t* ub = stages + static_cast<size_t>(slot) * stage_stride + j * ss + (pos >> 1) * C::ub;
             float acc;
             if constexpr (QT == 0)
                 acc = dot_q8_0_half_xr(ub + 136 * (pos & 1), xr, xfac);
