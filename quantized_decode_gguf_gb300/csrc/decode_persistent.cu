@@ -150,7 +150,9 @@ __global__ void __launch_bounds__(KCfg<QT, kCW>::threads, 1) decode_persistent_k
                 int nmat, segs;
                 int64_t row0;
                 if (!op_tile(op, t, nmat, row0, segs)) continue;
-                if (!produce_segs<QT, NS>(t, nmat, segs, smem, p.stage_stride, full, empty, s, pol)) break;
+                if (!produce_segs<KCfg<QT, kCW, NS>>(t, nmat, segs, seg_stride_bytes(t.useg, KCfg<QT, kCW, NS>::ub),
+                                                     smem, p.stage_stride, full, empty, s, pol))
+                    break;
             }
         }
         return;

@@ -131,6 +131,44 @@ __device__ __forceinline__ bool produce_tile(const Tile& t, int nmat, uint8_t* s
     return true;
 }
 
+// Segment-major stages (the register-resident kernels): a stage holds whole
+// row segments (one row of one matrix each; gate and up rows alternate when
+// nmat == 2) ss bytes apart. With consecutive threads on consecutive
+// segments at one half-unit position, segments whose length is a multiple of
+// 64 bytes get a 16-byte pad, so that those threads' weight reads spread over
+// the shared-memory banks.
+__host__ __device__ constexpr int seg_stride_bytes(int useg, int ub) {
+    return useg * ub + (((useg * ub) & 63) == 0 ? 16 : 0);
+}
+
+// Producer of segment-major stages: the tile's segments in order, segs per
+// stage, each at its place; one copy per stage when the rows are unpadded.
+template <class C>
+__device__ __forceinline__ bool produce_segs(const Tile& t, int nmat, int segs, int ss, uint8_t* stages,
+                                             uint32_t stage_stride, uint64_t* full, uint64_t* empty, int& s,
+                                             uint64_t pol) {
+    const int nseg = nmat * t.rows_here;
+    const int seg_bytes = t.useg * C::ub;
+    for (int seg0 = 0; seg0 < nseg; seg0 += segs, ++s) {
+        const int slot = s % C::ns;
+        if (s >= C::ns && !mbar_wait(&empty[slot], ((s / C::ns) - 1) & 1, &g_dev_err)) return false;
+        const int n = min(segs, nseg - seg0);
+        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(n * seg_bytes));
+        uint8_t* dst = stages + static_cast<size_t>(slot) * stage_stride;
+        if (nmat == 1 && ss == seg_bytes) {
+            bulk_g2s_hint(dst, t.w[0] + static_cast<int64_t>(seg0) * t.row_bytes, static_cast<uint32_t>(n * seg_bytes),
+                          &full[slot], pol);
+            continue;
+        }
+        for (int j = 0; j < n; ++j) {
+            const int seg = seg0 + j, r = seg / nmat, mat = seg - r * nmat;
+            bulk_g2s_hint(dst + j * ss, (mat == 0 ? t.w[0] : t.w[1]) + static_cast<int64_t>(r) * t.row_bytes,
+                          static_cast<uint32_t>(seg_bytes), &full[slot], pol);
+        }
+    }
+    return true;
+}
+
 // Consumers: dot every staged half unit with the activations and hand each
 // finished row to epi(r, b, a0, a1) for b < batch, with a0 the row's sum
 // (the gate row's for NMAT == 2) and a1 the up row's sum. `mode` is the

@@ -5,8 +5,12 @@
 // reduction. At batch 1 both show: the dot runs at about half the rate of a
 // dot whose activations sit in registers, and staging costs two barriers.
 // Here every stage holds whole row segments (a gate/up pair counting as
-// two), so consumer thread t works on segment t / (2 useg) and on the same
-// half-unit position pos = t % (2 useg) of every stage. The CTA reads x once
+// two), so a consumer thread works on the same half-unit position of every
+// stage: for rows of more than 16 half units thread t takes segment t % segs
+// at position t / segs (a warp's threads share few positions, so their
+// register fills are mostly broadcasts; segments are padded in the stage as
+// seg_stride_bytes says), for shorter rows segment t / (2 useg) at position
+// t % (2 useg) (the weight reads stay conflict-free). The CTA reads x once
 // (coalesced, each element once) into shared memory; after one barrier every
 // thread copies its 128 activations x[128 pos .. 128 pos + 127] into
 // registers, scaled by a power of two 2^s chosen from their own largest
@@ -50,6 +54,9 @@ struct XrParams {
     int useg;          // units per row (K / 256)
     int rows_per_cta;
     int segs;          // segments per stage
+    int segfast;       // 1: thread t on segment t % segs, position t / segs; 0: the reverse
+    int ss;            // bytes between a stage's segments
+    uint32_t stage_stride;
     const float* x;
     float* y;
     const uint8_t* pf[2];
@@ -92,7 +99,7 @@ __global__ void __launch_bounds__(32 * CW + 32, CW <= 6 ? 2 : 1) gemv_xr_kernel(
     if (tid >= C::consumers) {
         if (tid == C::consumers) {
             int s = 0;
-            produce_tile<QT, CW, kXrNS>(t, NMAT, smem, full, empty, s, policy_evict_first(), p.segs * t.useg);
+            produce_segs<C>(t, NMAT, p.segs, p.ss, smem, p.stage_stride, full, empty, s, policy_evict_first());
         } else if (tid == C::consumers + 1) {
             prefetch_share(p.pf[0], p.pf_bytes[0]);
             prefetch_share(p.pf[1], p.pf_bytes[1]);
@@ -101,8 +108,9 @@ __global__ void __launch_bounds__(32 * CW + 32, CW <= 6 ? 2 : 1) gemv_xr_kernel(
     }
 
     const int seg_half = 2 * t.useg;
-    const int j = tid / seg_half, pos = tid - j * seg_half;
-    const bool active = j < p.segs;
+    const int j = p.segfast ? tid % p.segs : tid / seg_half;
+    const int pos = p.segfast ? tid / p.segs : tid % seg_half;
+    const bool active = j < p.segs && pos < seg_half;
     pdl_wait();  // x may come from the previous kernel
     if (tid == 0) PHB_TRACE_EV(p.trace_id, 1);
     {
@@ -129,7 +137,7 @@ __global__ void __launch_bounds__(32 * CW + 32, CW <= 6 ? 2 : 1) gemv_xr_kernel(
         }
         const int seg = seg0 + j;
         if (active && seg < nseg) {
-            const uint8_t* ub = smem + slot * C::stage_bytes + (j * t.useg + (pos >> 1)) * C::ub;
+            const uint8_t* ub = smem + static_cast<size_t>(slot) * p.stage_stride + j * p.ss + (pos >> 1) * C::ub;
             float acc;
             if constexpr (QT == 0)
                 acc = dot_q8_0_half_xr(ub + 136 * (pos & 1), xr, xf);
@@ -187,6 +195,10 @@ cudaError_t gemv_xr_run(const GemvReq& q, cudaStream_t s) {
     p.n = q.n;
     p.useg = useg;
     p.segs = (consumers / (q.nmat * seg_half)) * q.nmat;
+    const int ub = q.qt == 0 ? Fmt<0>::unit_bytes : Fmt<1>::unit_bytes;
+    p.segfast = seg_half > 16 ? 1 : 0;
+    p.ss = p.segfast ? seg_stride_bytes(useg, ub) : useg * ub;
+    p.stage_stride = static_cast<uint32_t>((static_cast<size_t>(p.segs) * p.ss + 127) & ~size_t{127});
     const int64_t ctas = std::min<int64_t>(q.n, static_cast<int64_t>(device_sm_count()) * kXrCtasPerSm);
     p.rows_per_cta = static_cast<int>(cdiv(q.n, ctas));
     p.x = q.x;
@@ -196,8 +208,7 @@ cudaError_t gemv_xr_run(const GemvReq& q, cudaStream_t s) {
         p.pf[i] = static_cast<const uint8_t*>(q.pf[i]);
         p.pf_bytes[i] = q.pf_bytes[i];
     }
-    const size_t stage = static_cast<size_t>(16 * kXrCW) * (q.qt == 0 ? Fmt<0>::unit_bytes : Fmt<1>::unit_bytes);
-    size_t off = kXrNS * stage;
+    size_t off = kXrNS * static_cast<size_t>(p.stage_stride);
     p.xs_off = static_cast<uint32_t>(off);
     off += static_cast<size_t>(xpad_len(static_cast<int>(q.k))) * sizeof(float);
     p.part_off = static_cast<uint32_t>(off);

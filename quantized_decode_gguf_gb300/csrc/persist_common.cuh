@@ -268,50 +268,12 @@ __device__ __forceinline__ bool stage_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Row segments (whole rows of one matrix) lie in a stage seg_stride_bytes
-// apart: a segment's bytes, plus 16 when that length is a multiple of 128, so
-// that the segments start in different shared-memory bank groups (the
-// consumers read one half unit of many segments at once).
-__host__ __device__ constexpr int seg_stride_bytes(int useg, int ub) {
-    return useg * ub + (((useg * ub) & 127) == 0 ? 16 : 0);
-}
-
 // This thread's half-unit position within a row segment: consecutive threads
 // take consecutive segments at one position (segments fastest), so a warp's
 // threads share few positions and the register fill of their activations is
 // mostly broadcasts. Threads past segs * 2 useg get the last position (their
 // fill stays in range; they compute nothing).
 __device__ __forceinline__ int xr_pos(int segs, int useg) { return min(static_cast<int>(threadIdx.x) / segs, 2 * useg - 1); }
-
-// Producer of the persistent kernel: the tile's row segments in order, segs
-// per stage (gate and up rows alternate when nmat == 2), each at its padded
-// place; one copy per stage when the rows need no padding.
-template <int QT, int NS>
-__device__ __forceinline__ bool produce_segs(const Tile& t, int nmat, int segs, uint8_t* stages, uint32_t stage_stride,
-                                             uint64_t* full, uint64_t* empty, int& s, uint64_t pol) {
-    using C = KCfg<QT, kCW, NS>;
-    const int nseg = nmat * t.rows_here;
-    const int seg_bytes = t.useg * C::ub;
-    const int ss = seg_stride_bytes(t.useg, C::ub);
-    for (int seg0 = 0; seg0 < nseg; seg0 += segs, ++s) {
-        const int slot = s % C::ns;
-        if (s >= C::ns && !mbar_wait(&empty[slot], ((s / C::ns) - 1) & 1, &g_dev_err)) return false;
-        const int n = min(segs, nseg - seg0);
-        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(n * seg_bytes));
-        uint8_t* dst = stages + static_cast<size_t>(slot) * stage_stride;
-        if (nmat == 1 && ss == seg_bytes) {
-            bulk_g2s_hint(dst, t.w[0] + static_cast<int64_t>(seg0) * t.row_bytes, static_cast<uint32_t>(n * seg_bytes),
-                          &full[slot], pol);
-            continue;
-        }
-        for (int j = 0; j < n; ++j) {
-            const int seg = seg0 + j, r = seg / nmat, mat = seg - r * nmat;
-            bulk_g2s_hint(dst + j * ss, (mat == 0 ? t.w[0] : t.w[1]) + static_cast<int64_t>(r) * t.row_bytes,
-                          static_cast<uint32_t>(seg_bytes), &full[slot], pol);
-        }
-    }
-    return true;
-}
 
 // Consumers, activations in registers: dot every staged half unit of the
 // tile, park the half-unit sums in `part` (NMAT * rows_here * 2 useg
