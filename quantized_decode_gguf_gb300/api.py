@@ -223,10 +223,14 @@ def decode_workspace_size(qtype, d_model: int, n_q: int, n_kv: int, head_dim: in
 
 
 def layer_table(layers: Sequence[Sequence[torch.Tensor]]):
-    """Host array of phb_dense_layer from [(w_qkv, w_o, w_gate, w_up, w_down), ...]."""
+    """Host array of phb_dense_layer from [(w_qkv, w_o, w_gate, w_up, w_down), ...].
+
+    The array holds device pointers; it also keeps references to the tensors,
+    so that their memory cannot be freed and reused while the table exists."""
     arr = (_lib.DenseLayer * len(layers))()
     for i, ws in enumerate(layers):
         arr[i] = _lib.DenseLayer(*[_ptr(w) for w in ws])
+    arr._tensors = [list(ws) for ws in layers]
     return arr
 
 

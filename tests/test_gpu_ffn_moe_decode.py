@@ -38,6 +38,7 @@ FFN_CASES = [
     ("q4_k", 2048, 768, 1),    # one MoE expert
     ("q4_k", 2048, 768, 8),
     ("q4_k", 2560, 9728, 2),   # 4B-class FFN
+    ("q4_k", 3072, 1024, 1),   # gate/up pair on row segments fastest, padded in the stage
     ("q8_0", 96, 160, 3),      # generic (unfused) path: K % 256 != 0
     ("q4_k", 256, 512, 8),
     ("q8_0", 4096, 1024, 8),   # unfused: 8 * 4096 * 4 B > 80 KB of staged activations
@@ -202,6 +203,24 @@ D_MODEL, N_Q, N_KV, HD, D_FF = 2048, 16, 4, 128, 5632
 QKV = (N_Q + 2 * N_KV) * HD
 
 
+def test_layer_table_keeps_its_tensors_alive():
+    # the table holds raw device pointers; the binding keeps the tensors
+    # referenced, so a table built from temporaries cannot point at memory
+    # that was freed and reused (by the next allocation, a workspace say)
+    import gc
+    import weakref
+
+    tensors = [torch.zeros(64, dtype=torch.uint8, device="cuda") for _ in range(5)]
+    ref = weakref.ref(tensors[2])
+    table = phb.layer_table([tensors])
+    del tensors
+    gc.collect()
+    assert ref() is not None and table[0].w_gate == ref().data_ptr()
+    del table
+    gc.collect()
+    assert ref() is None
+
+
 def _layer_blobs(qtype, seed, layer):
     base = 5 * layer
     return [synth.blocks(qtype, seed, base + 0, QKV, D_MODEL), synth.blocks(qtype, seed, base + 1, D_MODEL, N_Q * HD),
@@ -235,6 +254,27 @@ def test_decode_single_layer_within_bound(qtype, fused):
     table = phb.layer_table([[to_dev(b) for b in blobs]])
     x = synth.normal_f32(600, 999, (D_MODEL,))
     check_decode_layer(qtype, table, _deq_layer(qtype, blobs), x, fused, f"decode layer {qtype} fused={fused}")
+    check_device_clean()
+
+
+@pytest.mark.parametrize("qtype", ["q8_0", "q4_k"])
+def test_decode_layer_other_shape_within_bound(qtype):
+    # d_model 1024, 8 query / 2 KV heads of 128, FFN 4096: every GEMV of the
+    # fused kernel has row segments of a multiple of 64 bytes (padded in the
+    # stage), the down projection included
+    d, nq, nkv, hd, ff = 1024, 8, 2, 128, 4096
+    qkv_n = (nq + 2 * nkv) * hd
+    shapes = [(qkv_n, d), (d, nq * hd), (ff, d), (ff, d), (d, ff)]
+    blobs = [synth.blocks(qtype, 620, i, r, c) for i, (r, c) in enumerate(shapes)]
+    mats = [oracle.dequant(qtype, b, r, c) for b, (r, c) in zip(blobs, shapes)]
+    table = phb.layer_table([[to_dev(b) for b in blobs]])
+    x = synth.normal_f32(620, 999, (d,))
+    for fused in (True, False):
+        ws = phb.decode_workspace(qtype, d, nq, nkv, hd, ff)
+        y = to_host(phb.decode_step(qtype, table, 1, d, nq, nkv, hd, ff, to_dev(x), ws=ws, fused=fused))
+        qkv, x1, act = (to_host(v) for v in phb.decode_step_probe(ws, d, nq, nkv, hd, ff, fused=fused))
+        st = oracle.decode_layer_stages(x, qkv, x1, act, *mats, nq, nkv, hd)
+        assert_stages(st, {"qkv": qkv, "x1": x1, "act": act, "out": y}, f"decode {qtype} d1024 fused={fused}")
     check_device_clean()
 
 
