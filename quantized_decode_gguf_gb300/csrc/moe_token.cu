@@ -347,10 +347,12 @@ __global__ void __launch_bounds__(kTokThreads, 1) moe_token_kernel(const __grid_
     const int pos2 = tid / rpass, jr = tid - pos2 * rpass;
     const int r = pos2 / sh_ff, hh = pos2 - r * sh_ff;
     const bool act2 = pos2 < p2;
+    // the activations into registers first: they do not wait for the down weights
+    float xr[128];
+    float xf = 1.f;
+    if (act2) xf = load_xr_scaled(hs + (r * sh_ff + hh) * (kXPadEvery + kXPad), xr);
     const bool okd = mbar_wait_warp(full_d, 0, &g_dev_err);
     if (okd && act2) {
-        float xr[128];
-        const float xf = load_xr_scaled(hs + (r * sh_ff + hh) * (kXPadEvery + kXPad), xr);
         for (int nl = jr; nl < rows_d; nl += rpass) {
             const uint8_t* unit = smem + p.wd_off + (static_cast<size_t>(r) * p.rd + nl) * p.rb_ff + (hh >> 1) * kUB;
             part[(nl * p.K + r) * sh_ff + hh] = half_dot<QT>(unit, hh & 1, xr, xf);
