@@ -169,4 +169,3 @@ def test_moe_tiered_rejects_bad_arguments(lib):
     tiered = lib.phb_moe_ffn_tiered_workspace_size(12, 16, 2048, 768, 128, 8)
     # the tiered workspace adds one staging slot per possible active expert (min(E, T*k) = 128)
     assert tiered >= plain + 128 * (2 * 768 * 1152 + 2048 * 432)
-
