@@ -6,11 +6,12 @@
 // dot whose activations sit in registers, and staging costs two barriers.
 // Here every stage holds whole row segments (a gate/up pair counting as
 // two), so a consumer thread works on the same half-unit position of every
-// stage: for rows of more than 16 half units thread t takes segment t % segs
-// at position t / segs (a warp's threads share few positions, so their
-// register fills are mostly broadcasts; segments are padded in the stage as
-// seg_stride_bytes says), for shorter rows segment t / (2 useg) at position
-// t % (2 useg) (the weight reads stay conflict-free). The CTA reads x once
+// stage: for Q4_K rows of more than 16 half units thread t takes segment
+// t % segs at position t / segs (a warp's threads share few positions, so
+// their register fills are mostly broadcasts; segments are padded in the
+// stage as seg_stride_bytes says), otherwise segment t / (2 useg) at
+// position t % (2 useg) (Q8_0's 8-byte weight reads stay conflict-free;
+// measured faster there). The CTA reads x once
 // (coalesced, each element once) into shared memory; after one barrier every
 // thread copies its 128 activations x[128 pos .. 128 pos + 127] into
 // registers, scaled by a power of two 2^s chosen from their own largest
@@ -196,7 +197,7 @@ cudaError_t gemv_xr_run(const GemvReq& q, cudaStream_t s) {
     p.useg = useg;
     p.segs = (consumers / (q.nmat * seg_half)) * q.nmat;
     const int ub = q.qt == 0 ? Fmt<0>::unit_bytes : Fmt<1>::unit_bytes;
-    p.segfast = seg_half > 16 ? 1 : 0;
+    p.segfast = (q.qt == 1 && seg_half > 16) ? 1 : 0;  // measured: Q8_0 rows gain nothing from it
     p.ss = p.segfast ? seg_stride_bytes(useg, ub) : useg * ub;
     p.stage_stride = static_cast<uint32_t>((static_cast<size_t>(p.segs) * p.ss + 127) & ~size_t{127});
     const int64_t ctas = std::min<int64_t>(q.n, static_cast<int64_t>(device_sm_count()) * kXrCtasPerSm);

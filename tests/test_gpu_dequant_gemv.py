@@ -72,8 +72,8 @@ GEMV_CASES = [
     ("q4_k", 9728, 2560, 4),
     ("q4_k", 2560, 9728, 4),      # K split at batch 4
     ("q4_k", 4096, 2560, 4),
-    ("q8_0", 1536, 4096, 1),      # batch 1, threads on row segments fastest, segments padded in the stage
-    ("q4_k", 1280, 3072, 1),      # the same for Q4_K (16 threads idle per stage)
+    ("q8_0", 1536, 4096, 1),      # batch 1, 32 half units per row
+    ("q4_k", 1280, 3072, 1),      # batch 1, threads on row segments fastest, segments padded (16 threads idle per stage)
     ("q4_k", 77, 256, 1),         # one super-block per row
     ("q4_k", 1000, 1280, 7),
     ("q4_k", 3, 512, 8),
