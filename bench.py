@@ -42,7 +42,7 @@ D_MODEL, N_Q, N_KV, HD, D_FF, N_LAYERS = 2048, 16, 4, 128, 5632, 24
 # DRAM bytes (read + write) per launch of the fused decode kernel at 24
 # layers: an ncu capture of the 4-layer case (191.75 MB read + 2.95 MB
 # written) scaled by 6; the weights are read once per step.
-DECODE_TRAFFIC_PER_LAUNCH = 6 * (191.762e6 + 3.130e6)
+DECODE_TRAFFIC_PER_LAUNCH = 6 * (191.746e6 + 3.146e6)
 QKV = (N_Q + 2 * N_KV) * HD
 LAYER_SHAPES = [("qkv", QKV, D_MODEL), ("o", D_MODEL, N_Q * HD), ("gate", D_FF, D_MODEL), ("up", D_FF, D_MODEL),
                 ("down", D_MODEL, D_FF)]

@@ -17,9 +17,8 @@
 // floor(176 / (nmat * useg)) * nmat segments (176 = half the consumer
 // threads) and thread t works on segment t % segs at half unit t / segs, so a
 // warp's threads share a few positions and fill their registers mostly by
-// broadcasts. Segments whose length is a multiple of 128 bytes are padded by
-// 16 bytes in the stage, so that the threads' weight reads at one position
-// spread over the shared-memory banks.
+// broadcasts. Segments are padded by 16 bytes in the stage, so that the
+// threads' weight reads at one position spread over the shared-memory banks.
 //
 // Readiness travels with the data. Every intermediate vector (qkv, x1, the
 // SwiGLU activation, each layer's output) is stored as 64-bit pairs

@@ -134,12 +134,12 @@ __device__ __forceinline__ bool produce_tile(const Tile& t, int nmat, uint8_t* s
 // Segment-major stages (the register-resident kernels): a stage holds whole
 // row segments (one row of one matrix each; gate and up rows alternate when
 // nmat == 2) ss bytes apart. With consecutive threads on consecutive
-// segments at one half-unit position, segments whose length is a multiple of
-// 64 bytes get a 16-byte pad, so that those threads' weight reads spread over
-// the shared-memory banks.
-__host__ __device__ constexpr int seg_stride_bytes(int useg, int ub) {
-    return useg * ub + (((useg * ub) & 63) == 0 ? 16 : 0);
-}
+// segments at one half-unit position, every segment gets a 16-byte pad, so
+// that those threads' weight reads spread over the shared-memory banks
+// (measured better than padding only segments of a multiple of 64 bytes:
+// Q4_K 9728x2560 batch-1 GEMV 7.17 -> 6.68 us, fused decode step
+// 0.528 -> 0.525 ms).
+__host__ __device__ constexpr int seg_stride_bytes(int useg, int ub) { return useg * ub + 16; }
 
 // Producer of segment-major stages: the tile's segments in order, segs per
 // stage, each at its place; one copy per stage when the rows are unpadded.
