@@ -6,12 +6,12 @@
 // dot whose activations sit in registers, and staging costs two barriers.
 // Here every stage holds whole row segments (a gate/up pair counting as
 // two), so a consumer thread works on the same half-unit position of every
-// stage: for Q4_K rows of more than 16 half units thread t takes segment
-// t % segs at position t / segs (a warp's threads share few positions, so
-// their register fills are mostly broadcasts; segments are padded in the
-// stage as seg_stride_bytes says), otherwise segment t / (2 useg) at
-// position t % (2 useg) (Q8_0's 8-byte weight reads stay conflict-free;
-// measured faster there). The CTA reads x once
+// stage: for rows of more than 16 half units, when a stage holds at least 8
+// row segments, thread t takes segment t % segs at position t / segs (a
+// warp's threads share few positions, so their register fills are mostly
+// broadcasts; segments are padded in the stage as seg_stride_bytes says),
+// otherwise segment t / (2 useg) at position t % (2 useg) (measured faster
+// for short rows and for stages of few long rows). The CTA reads x once
 // (coalesced, each element once) into shared memory; after one barrier every
 // thread copies its 128 activations x[128 pos .. 128 pos + 127] into
 // registers, scaled by a power of two 2^s chosen from their own largest
@@ -197,7 +197,10 @@ cudaError_t gemv_xr_run(const GemvReq& q, cudaStream_t s) {
     p.useg = useg;
     p.segs = (consumers / (q.nmat * seg_half)) * q.nmat;
     const int ub = q.qt == 0 ? Fmt<0>::unit_bytes : Fmt<1>::unit_bytes;
-    p.segfast = (q.qt == 1 && seg_half > 16) ? 1 : 0;  // measured: Q8_0 rows gain nothing from it
+    // measured: segments fastest pays when a stage holds 8 segments or more
+    // (Q8_0 9728x2560 8.4 -> 7.8 us) and costs with fewer (Q8_0 2048x5632
+    // 6.0 -> 6.5 us); at 16 half units or less positions fastest is cheaper
+    p.segfast = (seg_half > 16 && p.segs >= 8) ? 1 : 0;
     p.ss = p.segfast ? seg_stride_bytes(useg, ub) : useg * ub;
     p.stage_stride = static_cast<uint32_t>((static_cast<size_t>(p.segs) * p.ss + 127) & ~size_t{127});
     const int64_t ctas = std::min<int64_t>(q.n, static_cast<int64_t>(device_sm_count()) * kXrCtasPerSm);

@@ -72,8 +72,9 @@ GEMV_CASES = [
     ("q4_k", 9728, 2560, 4),
     ("q4_k", 2560, 9728, 4),      # K split at batch 4
     ("q4_k", 4096, 2560, 4),
-    ("q8_0", 1536, 4096, 1),      # batch 1, 32 half units per row
-    ("q4_k", 1280, 3072, 1),      # batch 1, threads on row segments fastest, segments padded (16 threads idle per stage)
+    ("q8_0", 1536, 4096, 1),      # batch 1, 32 half units per row, 5 rows per stage: positions fastest
+    ("q8_0", 1000, 2560, 1),      # batch 1, 8 rows per stage: threads on row segments fastest, padded
+    ("q4_k", 1280, 3072, 1),      # batch 1, 6 rows per stage (16 threads idle per stage)
     ("q4_k", 77, 256, 1),         # one super-block per row
     ("q4_k", 1000, 1280, 7),
     ("q4_k", 3, 512, 8),
