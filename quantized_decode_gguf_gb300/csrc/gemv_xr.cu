@@ -171,9 +171,10 @@ cudaError_t launch_xr(const XrParams& p, dim3 grid, size_t smem, cudaStream_t s,
     return launch_kernel(kern, grid, dim3(32 * CW + 32), smem, s, pdl, p);
 }
 
-// Consumer warps per CTA and CTAs per SM of the register-resident kernel.
+// Consumer warps per CTA of the register-resident kernel: five (two CTAs per
+// SM), or ten (one CTA per SM) for rows of more than 16 half units.
 constexpr int kXrCW = 5;
-constexpr int kXrCtasPerSm = 2;
+constexpr int kXrCWLong = 10;
 
 }  // namespace
 
@@ -188,40 +189,63 @@ cudaError_t gemv_xr_run(const GemvReq& q, cudaStream_t s) {
     if (!gemv_xr_fits(q)) return cudaErrorInvalidValue;
     const int useg = static_cast<int>(q.k / kUnitWeights);
     const int seg_half = 2 * useg;
-    const int consumers = 32 * kXrCW;
-    XrParams p{};
-    p.w[0] = static_cast<const uint8_t*>(q.w0);
-    p.w[1] = static_cast<const uint8_t*>(q.nmat == 2 ? q.w1 : q.w0);
-    p.row_bytes = static_cast<int64_t>(useg) * (q.qt == 0 ? Fmt<0>::unit_bytes : Fmt<1>::unit_bytes);
-    p.n = q.n;
-    p.useg = useg;
-    p.segs = (consumers / (q.nmat * seg_half)) * q.nmat;
     const int ub = q.qt == 0 ? Fmt<0>::unit_bytes : Fmt<1>::unit_bytes;
-    // measured: segments fastest pays when a stage holds 8 segments or more
-    // (Q8_0 9728x2560 8.4 -> 7.8 us) and costs with fewer (Q8_0 2048x5632
-    // 6.0 -> 6.5 us); at 16 half units or less positions fastest is cheaper
-    p.segfast = (seg_half > 16 && p.segs >= 8) ? 1 : 0;
-    p.ss = p.segfast ? seg_stride_bytes(useg, ub) : useg * ub;
-    p.stage_stride = static_cast<uint32_t>((static_cast<size_t>(p.segs) * p.ss + 127) & ~size_t{127});
-    const int64_t ctas = std::min<int64_t>(q.n, static_cast<int64_t>(device_sm_count()) * kXrCtasPerSm);
-    p.rows_per_cta = static_cast<int>(cdiv(q.n, ctas));
-    p.x = q.x;
-    p.y = q.y;
-    p.trace_id = q.trace_id;
-    for (int i = 0; i < 2; ++i) {
-        p.pf[i] = static_cast<const uint8_t*>(q.pf[i]);
-        p.pf_bytes[i] = q.pf_bytes[i];
-    }
-    size_t off = kXrNS * static_cast<size_t>(p.stage_stride);
-    p.xs_off = static_cast<uint32_t>(off);
-    off += static_cast<size_t>(xpad_len(static_cast<int>(q.k))) * sizeof(float);
-    p.part_off = static_cast<uint32_t>(off);
-    off += static_cast<size_t>(q.nmat) * p.rows_per_cta * seg_half * sizeof(float);
-    off = (off + 15) & ~size_t{15};
-    p.bar_off = static_cast<uint32_t>(off);
-    off += 2 * kXrNS * sizeof(uint64_t);
-    if (off > kSmemOptin) return cudaErrorInvalidConfiguration;
+    // The launch for cw consumer warps per CTA (two CTAs per SM at 5, one at
+    // 10); false if its shared memory does not fit.
+    auto plan = [&](int cw, XrParams& p, size_t& off) {
+        const int consumers = 32 * cw;
+        p = XrParams{};
+        p.w[0] = static_cast<const uint8_t*>(q.w0);
+        p.w[1] = static_cast<const uint8_t*>(q.nmat == 2 ? q.w1 : q.w0);
+        p.row_bytes = static_cast<int64_t>(useg) * ub;
+        p.n = q.n;
+        p.useg = useg;
+        p.segs = (consumers / (q.nmat * seg_half)) * q.nmat;
+        // measured: segments fastest pays when a stage holds 8 segments or more
+        // (Q8_0 9728x2560 8.4 -> 7.8 us) and costs with fewer (Q8_0 2048x5632
+        // 6.0 -> 6.5 us); at 16 half units or less positions fastest is cheaper
+        p.segfast = (seg_half > 16 && p.segs >= 8) ? 1 : 0;
+        p.ss = p.segfast ? seg_stride_bytes(useg, ub) : useg * ub;
+        p.stage_stride = static_cast<uint32_t>((static_cast<size_t>(p.segs) * p.ss + 127) & ~size_t{127});
+        const int ctas_per_sm = cw <= 6 ? 2 : 1;
+        const int64_t ctas = std::min<int64_t>(q.n, static_cast<int64_t>(device_sm_count()) * ctas_per_sm);
+        p.rows_per_cta = static_cast<int>(cdiv(q.n, ctas));
+        p.x = q.x;
+        p.y = q.y;
+        p.trace_id = q.trace_id;
+        for (int i = 0; i < 2; ++i) {
+            p.pf[i] = static_cast<const uint8_t*>(q.pf[i]);
+            p.pf_bytes[i] = q.pf_bytes[i];
+        }
+        off = kXrNS * static_cast<size_t>(p.stage_stride);
+        p.xs_off = static_cast<uint32_t>(off);
+        off += static_cast<size_t>(xpad_len(static_cast<int>(q.k))) * sizeof(float);
+        p.part_off = static_cast<uint32_t>(off);
+        off += static_cast<size_t>(q.nmat) * p.rows_per_cta * seg_half * sizeof(float);
+        off = (off + 15) & ~size_t{15};
+        p.bar_off = static_cast<uint32_t>(off);
+        off += 2 * kXrNS * sizeof(uint64_t);
+        return off <= kSmemOptin;
+    };
+    // measured: rows of more than 16 half units run faster as one CTA of ten
+    // consumer warps per SM (Q4_K 9728x2560 6.62 -> 6.41 us, Q8_0 2048x5632
+    // 6.15 -> 5.76 us), shorter ones as two CTAs of five (Q8_0 3072x2048
+    // 4.20 against 4.35 us)
+    XrParams p;
+    size_t off = 0;
+    int cw = kXrCW;
+    if (seg_half > 16 && plan(kXrCWLong, p, off))
+        cw = kXrCWLong;
+    else if (!plan(kXrCW, p, off))
+        return cudaErrorInvalidConfiguration;
     const dim3 grid(static_cast<unsigned>(cdiv(q.n, p.rows_per_cta)));
+    if (cw == kXrCWLong) {
+        if (q.qt == 0)
+            return q.nmat == 2 ? launch_xr<0, 2, kXrCWLong>(p, grid, off, s, q.pdl)
+                               : launch_xr<0, 1, kXrCWLong>(p, grid, off, s, q.pdl);
+        return q.nmat == 2 ? launch_xr<1, 2, kXrCWLong>(p, grid, off, s, q.pdl)
+                           : launch_xr<1, 1, kXrCWLong>(p, grid, off, s, q.pdl);
+    }
     if (q.qt == 0)
         return q.nmat == 2 ? launch_xr<0, 2, kXrCW>(p, grid, off, s, q.pdl) : launch_xr<0, 1, kXrCW>(p, grid, off, s, q.pdl);
     return q.nmat == 2 ? launch_xr<1, 2, kXrCW>(p, grid, off, s, q.pdl) : launch_xr<1, 1, kXrCW>(p, grid, off, s, q.pdl);
