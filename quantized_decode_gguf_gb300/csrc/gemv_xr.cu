@@ -22,8 +22,10 @@
 // that hold x: measured several times slower.)
 //
 // Half-unit sums go to shared memory; after the last stage one thread per row
-// adds them in position order (deterministic) and runs the epilogue: store,
-// or silu(gate) * up for the fused pair. A producer warp streams the CTA's
+// adds them in row_sum's fixed order (deterministic) and runs the epilogue:
+// store, or silu(gate) * up for the fused pair. Rows of more than 16 half
+// units run one CTA of ten consumer warps per SM, shorter rows two CTAs of
+// five (both measured faster that way). A producer warp streams the CTA's
 // row slice through a ring of stages with bulk copies (before the
 // programmatic-dependent-launch wait: weights never depend on the previous
 // kernel) and optionally prefetches later kernels' weights into L2.
